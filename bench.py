@@ -1,0 +1,557 @@
+"""Throughput benchmark of the GB300 FP8 scaled-quantization library.
+
+One step = one pass of the whole hot path over the five synthetic workloads
+(each kernel of the library runs in it):
+  W1 current scaling E4M3, BF16 1024x1024               amax(+scale) -> quantize
+  W2 current scaling cast+transpose E4M3, 8192x8192     amax(+scale) -> cast_transpose
+  W3 delayed scaling E4M3, 16 steps of 4096x14336       (quantize + amax + sat) -> update, x16
+  W4 blockwise E4M3, 128x128 on 7168x18432, 1x128 on 16384x7168
+  W5 E5M2 current scaling + dequantize, 32 x 8192x8192
+value = algorithmic bytes (each kernel's reads once + writes once) / time, in
+GB/s, with inputs resident in HBM.  The inputs (~6.5 GB) and the step's
+traffic (~21 GB) are far larger than the 126 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workloads (the method has no other implementation
+to compare with).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s (bytes read+written) and % of GB300 HBM peak per cast variant"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_NAME = ("fp8 scaled-quantization suite: W1 current E4M3 1024x1024; W2 current cast+transpose E4M3 "
+                 "8192x8192 margin 1; W3 delayed E4M3 16 x 4096x14336 hist 1024; W4 block E4M3 128x128 "
+                 "7168x18432 + 1x128 16384x7168; W5 current E5M2 quantize+dequantize 32 x 8192x8192")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="shrink every workload's row count by this factor (testing only; 1.0 = full size)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-fraction", type=float, default=1.0 / 16,
+                    help="fraction of each workload the CPU-oracle baseline processes")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- workloads
+
+def workload_shapes(scale: float):
+    from fp8_scaled_quantization_gb300 import workloads as wl
+
+    def s(shape, mult=128):
+        r = max(mult, int(shape[0] * scale) // mult * mult)
+        return (r, shape[1])
+
+    return {
+        "w1": wl.W1_SHAPE,
+        "w2": s(wl.W2_SHAPE),
+        "w3": s(wl.W3_SHAPE),
+        "w4w": s(wl.W4_WEIGHT_SHAPE),
+        "w4a": s(wl.W4_ACT_SHAPE),
+        "w5": s(wl.W5_SHAPE),
+        "w3_steps": wl.W3_STEPS,
+        "w5_count": wl.W5_TENSORS,
+    }
+
+
+def make_inputs(shapes, device, seed_offset=0):
+    from fp8_scaled_quantization_gb300 import workloads as wl
+    S = wl.SEEDS
+    x1 = wl.w1_outliers(shapes["w1"], device, seed=S["w1"] + seed_offset)
+    x2 = wl.w2_student_t(shapes["w2"], device, seed=S["w2"] + seed_offset)
+    x3 = list(wl.w3_steps(shapes["w3"], shapes["w3_steps"], device, seed=S["w3"] + seed_offset))
+    w4, a4 = wl.w4_block(shapes["w4w"], shapes["w4a"], device, seed=S["w4"] + seed_offset)
+    x5 = list(wl.w5_gradients(shapes["w5"], shapes["w5_count"], device, seed=S["w5"] + seed_offset))
+    return {"w1": x1, "w2": x2, "w3": x3, "w4": (w4, a4), "w5": x5}
+
+
+def make_pipelines(inp):
+    from fp8_scaled_quantization_gb300 import pipelines as P, E4M3, E5M2
+    return {
+        "W1": P.CurrentScaling(inp["w1"], E4M3, 0),
+        "W2": P.CurrentCastTranspose(inp["w2"], E4M3, 1),
+        "W3": P.DelayedScaling(inp["w3"], 1024, E4M3, 0),
+        "W4": P.BlockScaling(*inp["w4"], E4M3),
+        "W5": P.GradientQDQ(inp["w5"], E5M2, 0),
+    }
+
+
+# --------------------------------------------------------------------- timing
+
+class EventTimer:
+    """CUDA events around each launch, per kernel name (current stream)."""
+
+    def __init__(self):
+        import torch
+        self.torch = torch
+        self.pool = []
+        self.spans = {}
+        self.open = {}
+
+    def _ev(self):
+        return self.pool.pop() if self.pool else self.torch.cuda.Event(enable_timing=True)
+
+    def reserve(self, n):
+        self.pool.extend(self.torch.cuda.Event(enable_timing=True) for _ in range(n))
+
+    def start(self, name):
+        e = self._ev()
+        e.record()
+        self.open[name] = e
+
+    def stop(self, name):
+        e = self._ev()
+        e.record()
+        self.spans.setdefault(name, []).append((self.open.pop(name), e))
+
+    def totals(self):
+        """name -> (total ms, launches); call after a synchronize."""
+        return {k: (sum(a.elapsed_time(b) for a, b in v), len(v)) for k, v in self.spans.items()}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc, self.path, self.gpu_id = None, None, gpu_id
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() in ("active", "1", "yes")})
+        load = [v for v in sm if v and mx and v > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per element from the committed ncu summary, when it was taken
+    on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = {"quantize": "quantize.cu", "cast_transpose": "cast_transpose.cu", "amax": "amax_scale.cu",
+           "dequantize": "dequantize.cu", "block128x128": "block_quant.cu", "block1x128": "block_quant.cu"}.get(kernel)
+    if src is None or not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in (src, "fp8q_device.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_scaled_quantization_gb300", "csrc", f), "rb").read())
+    digest = h.hexdigest()[:16]
+    for line in open(path):
+        m = dict(re.findall(r"(\w+)=(\S+)", line))
+        if m.get("kernel") == kernel and m.get("source_sha") == digest:
+            return float(m["dram_bytes_per_element"])
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import fp8_scaled_quantization_gb300 as fq
+    from fp8_scaled_quantization_gb300.pipelines import KernelBytes
+
+    fq.library()  # raises if the CUDA library is missing: there is no fallback
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    shapes = workload_shapes(args.scale)
+    inp = make_inputs(shapes, dev, seed_offset=rank)
+    pipes = make_pipelines(inp)
+    per_variant_bytes = {k: p.bytes() for k, p in pipes.items()}
+    kb = KernelBytes()
+    for b in per_variant_bytes.values():
+        for name, (nbytes, launches) in b.per_kernel.items():
+            kb.add(name, nbytes // launches, launches)
+    step_bytes = kb.total
+    torch.cuda.synchronize()
+
+    def step(timer=None, vt=None):
+        for name, p in pipes.items():
+            if vt is not None:
+                vt.start(name)
+            p.run(timer)
+            if vt is not None:
+                vt.stop(name)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    timer, vtimer = EventTimer(), EventTimer()
+    timer.reserve(2 * kb.launches * args.steps + 8)
+    vtimer.reserve(2 * len(pipes) * args.steps + 8)
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    launches0 = fq.launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step(timer, vtimer)
+    t1.record()
+    torch.cuda.synchronize()
+    launches = fq.launch_count() - launches0
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, world)
+
+    peak, peak_kind = measured_hbm_peak()
+    kernels = {}
+    for name, (tot_ms, n) in timer.totals().items():
+        nbytes, nl = kb.per_kernel[name]
+        nbytes_run = nbytes * args.steps
+        gbs = nbytes_run / (tot_ms * 1e-3) / 1e9
+        kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": tot_ms / args.steps,
+                         "avg_launch_us": tot_ms * 1e3 / n, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    dominant = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    dk = kernels[dominant]
+    variants = {}
+    for name, (tot_ms, n) in vtimer.totals().items():
+        b = per_variant_bytes[name].total
+        gbs = b * args.steps / (tot_ms * 1e-3) / 1e9
+        variants[name] = {"bytes_per_step": b, "ms_per_step": round(tot_ms / args.steps, 4), "gbs": round(gbs, 1),
+                          "frac": round(gbs / peak, 4)}
+    traffic_per_elem = kernel_traffic(dominant)
+    elems_per_launch = None
+    if traffic_per_elem is not None:
+        per_elem_bytes = {"quantize": 3, "cast_transpose": 4, "amax": 2, "dequantize": 3}.get(dominant)
+        if per_elem_bytes:
+            elems_per_launch = dk["bytes_per_step"] / dk["launches_per_step"] / per_elem_bytes
+    value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "io": "bf16 in, e4m3/e5m2 uint8 codes out (W5: bf16 out)",
+                   "bytes_per_step": step_bytes, "row_scale": args.scale,
+                   "l2": "no flush: inputs (%.1f GB) and per-step traffic (%.1f GB) exceed the 126 MB L2"
+                         % (sum(t.numel() * t.element_size() for t in _all_inputs(inp)) / 1e9, step_bytes / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": round(dk["gbs"] / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": (round(traffic_per_elem * elems_per_launch) if elems_per_launch else None),
+                     "algorithmic_bytes_per_launch": round(dk["bytes_per_step"] / dk["launches_per_step"])},
+        "kernels": kernels,
+        "variants": variants,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, pipes, inp, step_bytes, world)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args, inp)
+    return result
+
+
+def _all_inputs(inp):
+    out = [inp["w1"], inp["w2"], *inp["w3"], *inp["w4"], *inp["w5"]]
+    return out
+
+
+def _outputs(pipes):
+    """The results a caller reads back: codes and scales (W5: the BF16 dequantized tensors)."""
+    p1, p2, p3, p4, p5 = (pipes[k] for k in ("W1", "W2", "W3", "W4", "W5"))
+    return {
+        "W1": [p1.q, p1.scale_inv],
+        "W2": [p2.q_row, p2.q_col, p2.scale_inv],
+        "W3": [p3.q[0], p3.amax, p3.sat, p3.scale_inv],
+        "W4": [p4.q_w, p4.si_w, p4.q_a, p4.si_a],
+        "W5": [p5.y[0], p5.scale_inv],
+    }
+
+
+def run_e2e(args, pipes, inp, step_bytes, world):
+    """The same step through the public API from pinned host memory: every step
+    copies its inputs host->device and reads its results device->host."""
+    import torch
+    ins = {"W1": [inp["w1"]], "W2": [inp["w2"]], "W3": inp["w3"], "W4": list(inp["w4"]), "W5": inp["w5"]}
+    h_in = {k: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in v] for k, v in ins.items()}
+    for k, v in ins.items():
+        for h, d in zip(h_in[k], v):
+            h.copy_(d)
+    outs = _outputs(pipes)
+    # W3 and W5 reuse one output buffer per step / tensor, so their results are read after each one
+    h_out = {k: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in v] for k, v in outs.items()}
+    h3 = [torch.empty(pipes["W3"].q[0].shape, dtype=torch.uint8, pin_memory=True) for _ in inp["w3"]]
+    h5 = [torch.empty(pipes["W5"].y[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in inp["w5"]]
+    h2d = sum(t.numel() * t.element_size() for v in h_in.values() for t in v)
+    d2h = sum(t.numel() * t.element_size() for v in h_out.values() for t in v) + \
+        sum(t.numel() for t in h3[1:]) + sum(t.numel() * 2 for t in h5[1:])
+
+    def e2e_step():
+        for k in ("W1", "W2", "W4"):
+            for h, d in zip(h_in[k], ins[k]):
+                d.copy_(h, non_blocking=True)
+            pipes[k].run()
+            for h, d in zip(h_out[k], outs[k]):
+                h.copy_(d, non_blocking=True)
+        p3 = pipes["W3"]
+        for h, d in zip(h_in["W3"], ins["W3"]):
+            d.copy_(h, non_blocking=True)
+        p3.hist.zero_()
+        from fp8_scaled_quantization_gb300 import fp8_quantize, fp8_update_scale_delayed
+        fp8_update_scale_delayed(p3.hist, 0, None, p3.algo, p3.fmt, p3.margin, p3.scale, p3.scale_inv)
+        for k, x in enumerate(p3.xs):
+            fp8_quantize(x, p3.fmt, p3.scale, p3.q[0], p3.amax[k:k + 1], p3.sat[k:k + 1])
+            h3[k].copy_(p3.q[0], non_blocking=True)
+            fp8_update_scale_delayed(p3.hist, k, p3.amax[k:k + 1], p3.algo, p3.fmt, p3.margin, p3.scale,
+                                     p3.scale_inv)
+        for h, d in zip(h_out["W3"][1:], outs["W3"][1:]):
+            h.copy_(d, non_blocking=True)
+        p5 = pipes["W5"]
+        from fp8_scaled_quantization_gb300 import fp8_amax, fp8_dequantize
+        for k, (h, x) in enumerate(zip(h_in["W5"], p5.xs)):
+            x.copy_(h, non_blocking=True)
+            s, si = p5.scale[k:k + 1], p5.scale_inv[k:k + 1]
+            fp8_amax(x, p5.amax[k:k + 1], p5.fmt, p5.margin, s, si)
+            fp8_quantize(x, p5.fmt, s, p5.q[0])
+            fp8_dequantize(p5.q[0], p5.fmt, si, p5.y[0])
+            h5[k].copy_(p5.y[0], non_blocking=True)
+        h_out["W5"][1].copy_(p5.scale_inv, non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    dt = max_over_ranks((time.perf_counter() - t) * 1e3, world)
+    return {"value": round(world * step_bytes * steps / (dt * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(dt / steps, 3),
+            "note": "pinned host buffers, one stream, copies serialised with the kernels"}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_suite_sample(inp_host, fraction, threads):
+    """Run the oracle over a sample of every workload; returns algorithmic bytes."""
+    import numpy as np
+    import oracle as O
+
+    def rows(x, f):
+        r = max(1, int(x.shape[0] * f))
+        return np.ascontiguousarray(x[:r])
+
+    nbytes = 0
+    x1 = inp_host["w1"]
+    s, si = O.compute_scale(O.amax(x1, threads), O.E4M3, 0)
+    O.quantize(x1, O.E4M3, s, threads)
+    nbytes += x1.size * 5
+    x2 = rows(inp_host["w2"], fraction)
+    s, si = O.compute_scale(O.amax(x2, threads), O.E4M3, 1)
+    O.cast_transpose(x2, O.E4M3, s, threads)
+    nbytes += x2.size * 6
+    hist = np.zeros(1024, np.float32)
+    s, si = O.update_delayed(hist, 0, None, O.ALGO_MAX, O.E4M3, 0)
+    for k, x in enumerate(inp_host["w3"]):
+        x = rows(x, fraction)
+        O.quantize(x, O.E4M3, s, threads)
+        s, si = O.update_delayed(hist, k, O.amax(x, threads), O.ALGO_MAX, O.E4M3, 0)
+        nbytes += x.size * 3
+    w, a = inp_host["w4"]
+    w = rows(w, fraction)
+    w = w[: max(128, w.shape[0] // 128 * 128)]
+    O.quantize_block(np.ascontiguousarray(w), 128, 128, O.E4M3, threads)
+    a = rows(a, fraction)
+    O.quantize_block(a, 1, 128, O.E4M3, threads)
+    nbytes += w.size * 3 + a.size * 3
+    for x in inp_host["w5"]:
+        x = rows(x, fraction)
+        s, si = O.compute_scale(O.amax(x, threads), O.E5M2, 0)
+        q, _ = O.quantize(x, O.E5M2, s, threads)
+        O.dequantize(q, O.E5M2, np.array([si], np.float32), threads=threads)
+        nbytes += x.size * 8
+    return nbytes
+
+
+def host_sample(inp, fraction, max_w3=4, max_w5=4):
+    """Host copies of the leading rows of each workload tensor (a bounded sample)."""
+    from fp8_scaled_quantization_gb300.workloads import bf16_bits
+
+    def r(x):
+        return bf16_bits(x[: max(1, int(x.shape[0] * fraction))])
+
+    return {"w1": bf16_bits(inp["w1"]), "w2": r(inp["w2"]), "w3": [r(x) for x in inp["w3"][:max_w3]],
+            "w4": (r(inp["w4"][0]), r(inp["w4"][1])), "w5": [r(x) for x in inp["w5"][:max_w5]]}
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args, inp):
+    import oracle as O
+    O.build()
+    sample = host_sample(inp, args.cpu_fraction)
+    threads = cpu_threads()
+    t = time.perf_counter()
+    nbytes = oracle_suite_sample(sample, 1.0, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"leading {args.cpu_fraction:.4g} of the rows of W2, W3 (4 of 16 steps), W4, W5 (4 of 32 "
+                      f"tensors) and all of W1; the oracle's own algorithmic bytes ({nbytes / 1e9:.2f} GB)"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on a bounded sample of each workload."""
+    import oracle as O
+    import torch
+    from fp8_scaled_quantization_gb300 import workloads as wl
+    O.build()
+    shapes = workload_shapes(args.scale)
+    f = 1.0 / 64
+    shp = lambda s: (max(128, int(s[0] * f) // 128 * 128), s[1])  # noqa: E731
+    inp = {"w1": wl.w1_outliers(shapes["w1"]), "w2": wl.w2_student_t(shp(shapes["w2"])),
+           "w3": list(wl.w3_steps(shp(shapes["w3"]), 4)),
+           "w4": wl.w4_block(shp(shapes["w4w"]), shp(shapes["w4a"])),
+           "w5": list(wl.w5_gradients(shp(shapes["w5"]), 4))}
+    sample = host_sample(inp, 1.0)
+    threads = cpu_threads()
+    torch.set_num_threads(max(1, threads))
+    for _ in range(args.warmup):
+        oracle_suite_sample(sample, 1.0, threads)
+    t = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_suite_sample(sample, 1.0, threads)
+    dt = time.perf_counter() - t
+    v = round(nbytes / dt / 1e9, 3)
+    desc = ("each step: the oracle on 1/64 of the rows of W2, 4 of 16 W3 steps, W4, 4 of 32 W5 tensors, and "
+            "all of W1 (CPU-generated inputs of the same distributions)")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "sample": desc},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------- plumbing
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle runs once, on rank 0; other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference(args, 0, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend)
+    res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

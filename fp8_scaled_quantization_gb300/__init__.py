@@ -1,0 +1,155 @@
+"""GB300-native FP8 scaled quantization.
+
+Python binding of the C ABI in ``include/fp8q.h``.  Every function here only
+marshals arguments (tensor data pointers, sizes, the current CUDA stream) and
+calls the CUDA library; all arithmetic runs in the library's sm_103a kernels.
+Tensors must be contiguous CUDA tensors; BF16 / fp32 inputs, uint8 codes,
+fp32 scalars, int64 saturation counters (read as unsigned 64-bit).
+
+Entry points (same names as the C ABI):
+  fp8_amax, fp8_update_scale_delayed, fp8_quantize,
+  fp8_quantize_cast_transpose, fp8_quantize_block, fp8_dequantize.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+E4M3, E5M2 = 0, 1
+DT_BF16, DT_FP32 = 0, 1
+AMAX_MAX, AMAX_MOST_RECENT = 0, 1
+FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+__all__ = [
+    "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
+    "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
+    "fp8_quantize_block", "fp8_dequantize", "launch_count", "version", "library",
+]
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} [status {status}]")
+        self.status = status
+
+
+def library():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _lib.load()
+
+
+def version() -> int:
+    return library().fp8_version()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(library().fp8_launch_count())
+
+
+def _check(status: int):
+    if status != 0:
+        msg = library().fp8_last_error_message().decode(errors="replace")
+        raise Fp8Error(status, msg)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    if t.dtype == torch.float32:
+        return DT_FP32
+    raise TypeError(f"expected a bfloat16 or float32 tensor, got {t.dtype}")
+
+
+def _p(t) -> int | None:
+    """Data pointer of an optional contiguous CUDA tensor."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a tensor, got {type(t)}")
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the FP8 library must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the FP8 library must be contiguous")
+    return t.data_ptr() or None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _rows_cols(x: torch.Tensor):
+    if x.dim() != 2:
+        raise ValueError(f"expected a 2-D tensor, got shape {tuple(x.shape)}")
+    return int(x.shape[0]), int(x.shape[1])
+
+
+def fp8_amax(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):
+    """amax_out[0] = max|x|; with scale_out / scale_inv_out, also the current scale."""
+    _check(library().fp8_amax(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
+                              _p(scale_out), _p(scale_inv_out), _stream(stream)))
+
+
+def fp8_update_scale_delayed(amax_history, step, new_amax, algo, fmt, margin, scale_out, scale_inv_out,
+                             stream=None):
+    """Delayed-scaling update of a float32 history (in place) -> scale_out, scale_inv_out."""
+    if amax_history.dtype != torch.float32:
+        raise TypeError("amax_history must be float32")
+    _check(library().fp8_update_scale_delayed(_p(amax_history), amax_history.numel(), int(step), _p(new_amax),
+                                              algo, fmt, margin, _p(scale_out), _p(scale_inv_out),
+                                              _stream(stream)))
+
+
+def fp8_quantize(x, fmt, scale, q_out, amax_out=None, sat_count_out=None, stream=None):
+    """q_out = FP8 codes of x * scale; optional fused amax and saturation count."""
+    if q_out.dtype != torch.uint8:
+        raise TypeError("q_out must be uint8")
+    if q_out.numel() != x.numel():
+        raise ValueError("q_out must have as many elements as x")
+    _check(library().fp8_quantize(_p(x), _dt(x), x.numel(), fmt, _p(scale), _p(q_out), _p(amax_out),
+                                  _p(sat_count_out), _stream(stream)))
+
+
+def fp8_quantize_cast_transpose(x, fmt, scale, q_row, q_col, amax_out=None, stream=None):
+    """Rowwise [rows, cols] and columnwise [cols, rows] codes under one scale."""
+    rows, cols = _rows_cols(x)
+    if q_row is not None and (q_row.dtype != torch.uint8 or tuple(q_row.shape) != (rows, cols)):
+        raise ValueError("q_row must be uint8 [rows, cols]")
+    if q_col is not None and (q_col.dtype != torch.uint8 or tuple(q_col.shape) != (cols, rows)):
+        raise ValueError("q_col must be uint8 [cols, rows]")
+    _check(library().fp8_quantize_cast_transpose(_p(x), _dt(x), rows, cols, fmt, _p(scale), _p(q_row),
+                                                 _p(q_col), _p(amax_out), _stream(stream)))
+
+
+def fp8_quantize_block(x, block_rows, block_cols, fmt, q_out, scale_inv_out, stream=None):
+    """Block-scaled codes and per-block scale_inv ([ceil(r/br), ceil(c/bc)] fp32)."""
+    rows, cols = _rows_cols(x)
+    if q_out.dtype != torch.uint8 or tuple(q_out.shape) != (rows, cols):
+        raise ValueError("q_out must be uint8 [rows, cols]")
+    if block_rows > 0 and block_cols > 0:
+        want = (-(-rows // block_rows), -(-cols // block_cols))
+        if scale_inv_out.dtype != torch.float32 or tuple(scale_inv_out.shape) != want:
+            raise ValueError(f"scale_inv_out must be float32 {want}")
+    _check(library().fp8_quantize_block(_p(x), _dt(x), rows, cols, block_rows, block_cols, fmt, _p(q_out),
+                                        _p(scale_inv_out), _stream(stream)))
+
+
+def fp8_dequantize(q, fmt, scale_inv, y, block_rows=0, block_cols=0, stream=None):
+    """y = decode(q) * scale_inv (fp32 multiply) stored as y's dtype (bf16 / fp32)."""
+    if q.dtype != torch.uint8:
+        raise TypeError("q must be uint8")
+    if y.numel() != q.numel():
+        raise ValueError("y must have as many elements as q")
+    if q.dim() == 2:
+        rows, cols = int(q.shape[0]), int(q.shape[1])
+    else:
+        if block_rows or block_cols:
+            raise ValueError("block-scaled dequantize needs a 2-D q")
+        rows, cols = 1, q.numel()
+    _check(library().fp8_dequantize(_p(q), fmt, rows, cols, _p(scale_inv), block_rows, block_cols, _p(y),
+                                    _dt(y), _stream(stream)))

@@ -1,0 +1,182 @@
+// amax_scale.cu -- amax reduction with fused current-scale finalize, and the
+// delayed-scaling history update.
+//
+// amax ("Megatron FP8" §4: a dedicated reduction kernel producing an fp32
+// scalar; §10: current scaling scans the tensor before the cast).  |x| of
+// BF16 is its bit pattern with the sign cleared; for non-negative floats the
+// unsigned order of the bits is the numeric order and NaN patterns sort above
+// Inf, so an unsigned 16-bit max (two lanes per 32-bit word) is an exact,
+// order-free, NaN-propagating amax.  CTAs fold their maximum into a 64-byte
+// workspace; the last CTA to arrive turns it into amax, scale and scale_inv
+// and resets the workspace, so one launch does the whole current-scaling
+// prologue.
+//
+// Delayed update ("Megatron FP8" §5, update_fp8_meta): one CTA writes the new
+// amax into slot step % len, takes the window maximum (or the slot, for
+// most_recent) and derives scale / scale_inv for the next cast.
+#include "fp8q_device.cuh"
+#include "fp8q_host.h"
+
+namespace fp8q {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+
+// x is 16-byte aligned here; `n` counts elements of width ESIZE from x.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+amax_kernel(const uint8_t* __restrict__ head, int head_n, const uint8_t* __restrict__ x, int64_t n,
+            Workspace* ws, FinishArgs fa) {
+    constexpr int kPer = BF16 ? 8 : 4;  // elements per 16-byte chunk
+    const int64_t nchunks = n / kPer;
+    uint32_t acc = 0;  // BF16: u16x2 lanes; fp32: f32 bits
+
+    const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nchunks; base += step) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int64_t c = base + (int64_t)k * kThreads;
+            v[k] = c < nchunks ? ldg_stream(x + c * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if constexpr (BF16) {
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
+                                               max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w))));
+            } else {
+                acc = umax(acc, umax(umax(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu),
+                                     umax(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu)));
+            }
+        }
+    }
+    uint32_t bits = BF16 ? fold_u16x2_to_f32bits(acc) : acc;
+
+    // Elements before the first 16-byte boundary and after the last chunk.
+    if (blockIdx.x == 0) {
+        const int64_t tail_start = nchunks * kPer;
+        const int64_t tail_n = n - tail_start;
+        for (int64_t i = threadIdx.x; i < head_n + tail_n; i += kThreads) {
+            const uint8_t* p = i < head_n ? head + i * (BF16 ? 2 : 4) : x + (tail_start + (i - head_n)) * (BF16 ? 2 : 4);
+            uint32_t b = BF16 ? ((uint32_t)(*reinterpret_cast<const uint16_t*>(p) & 0x7FFFu) << 16)
+                              : (*reinterpret_cast<const uint32_t*>(p) & 0x7FFFFFFFu);
+            bits = umax(bits, b);
+        }
+    }
+
+    __shared__ uint32_t red[32];
+    bits = block_max_u32(bits, red);
+    grid_finish(ws, bits, 0ull, fa);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(1024)
+update_delayed_kernel(float* hist, int len, int slot, const float* new_amax, int algo, int margin,
+                      float* scale_out, float* scale_inv_out) {
+    if (new_amax != nullptr && threadIdx.x == 0) hist[slot] = *new_amax;
+    __syncthreads();  // the slot write is visible to the whole CTA
+    float eff;
+    if (algo == FP8_AMAX_MOST_RECENT) {
+        eff = hist[slot];
+    } else {
+        // NaN-propagating maximum over the window.
+        float m = -INFINITY;
+        int saw_nan = 0;
+        for (int i = threadIdx.x; i < len; i += blockDim.x) {
+            float v = hist[i];
+            if (isnan(v)) saw_nan = 1;
+            else m = fmaxf(m, v);
+        }
+        saw_nan = __syncthreads_or(saw_nan);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        __shared__ float red[32];
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        eff = saw_nan ? __uint_as_float(0x7FC00000u) : m;
+    }
+    if (threadIdx.x == 0) {
+        float s, si;
+        scale_from_amax<FMT>(eff, margin, &s, &si);
+        *scale_out = s;
+        *scale_inv_out = si;
+    }
+}
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8_status_t fp8_amax(const void* x, fp8_dtype_t dtype, int64_t n, float* amax_out,
+                                 fp8_format_t fmt, int margin, float* scale_out, float* scale_inv_out,
+                                 void* stream) {
+    if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: unknown dtype %d", (int)dtype);
+    if (n < 0) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: n < 0");
+    if (n > 0 && x == nullptr) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: x is NULL");
+    if (amax_out == nullptr) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: amax_out is NULL");
+    if ((scale_out == nullptr) != (scale_inv_out == nullptr))
+        return fail(FP8_ERR_INVALID_ARG, "fp8_amax: scale_out and scale_inv_out must both be set or both NULL");
+    if (scale_out && !valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: unknown format %d", (int)fmt);
+    if (scale_out && !valid_margin(margin)) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: margin out of [-126, 126]");
+    const int es = dtype_size(dtype);
+    if (reinterpret_cast<uintptr_t>(x) % es) return fail(FP8_ERR_INVALID_ARG, "fp8_amax: x not element-aligned");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    fp8_status_t s;
+    Workspace* ws = stream_workspace(st, &s);
+    if (!ws) return s;
+
+    // Peel elements up to the first 16-byte boundary.
+    const uint8_t* p = static_cast<const uint8_t*>(x);
+    int64_t head = p ? (int64_t)(((16u - (reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) / es) : 0;
+    if (head > n) head = n;
+    const uint8_t* body = p ? p + head * es : p;
+    const int64_t body_n = n - head;
+
+    const int per = dtype == FP8_DT_BF16 ? 8 : 4;
+    const int64_t chunks = body_n / per;
+    int64_t grid = (chunks + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+
+    FinishArgs fa{amax_out, scale_out, scale_inv_out, nullptr, (int)fmt, margin};
+    if (dtype == FP8_DT_BF16)
+        amax_kernel<true><<<(unsigned)grid, kThreads, 0, st>>>(p, (int)head, body, body_n, ws, fa);
+    else
+        amax_kernel<false><<<(unsigned)grid, kThreads, 0, st>>>(p, (int)head, body, body_n, ws, fa);
+    return after_launch("fp8_amax");
+}
+
+extern "C" fp8_status_t fp8_update_scale_delayed(float* amax_history, int history_len, int64_t step,
+                                                 const float* new_amax, fp8_amax_algo_t algo,
+                                                 fp8_format_t fmt, int margin, float* scale_out,
+                                                 float* scale_inv_out, void* stream) {
+    if (amax_history == nullptr) return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: amax_history is NULL");
+    if (history_len < 1 || history_len > 65536)
+        return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: history_len must be in [1, 65536]");
+    if (step < 0) return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: step < 0");
+    if (algo != FP8_AMAX_MAX && algo != FP8_AMAX_MOST_RECENT)
+        return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: unknown algo %d", (int)algo);
+    if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: unknown format %d", (int)fmt);
+    if (!valid_margin(margin)) return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: margin out of [-126, 126]");
+    if (scale_out == nullptr || scale_inv_out == nullptr)
+        return fail(FP8_ERR_INVALID_ARG, "fp8_update_scale_delayed: scale_out / scale_inv_out is NULL");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int slot = (int)(step % history_len);
+    const int threads = history_len >= 1024 ? 1024 : (history_len >= 256 ? 256 : 32);
+    if (fmt == FP8_E4M3)
+        update_delayed_kernel<kE4M3><<<1, threads, 0, st>>>(amax_history, history_len, slot, new_amax, (int)algo,
+                                                            margin, scale_out, scale_inv_out);
+    else
+        update_delayed_kernel<kE5M2><<<1, threads, 0, st>>>(amax_history, history_len, slot, new_amax, (int)algo,
+                                                            margin, scale_out, scale_inv_out);
+    return after_launch("fp8_update_scale_delayed");
+}

@@ -1,0 +1,246 @@
+// block_quant.cu -- block-scaled quantize with one fp32 scale per 128 x 128
+// block or per 1 x 128 row tile; the stored factor is scale_inv.
+//
+// "Low Precision Training and Rollout": 128 x 128 block FP8 ("BF16 Training
+// with FP8 Rollout"), FP32 block scales ("FP8 Quick Start"), the inverse
+// scale stored per block ("MXFP8 (Blackwell only)", weight_scale_inv).  The
+// 1 x 128 tile is the activation-side Float8Blockwise shape of
+// "[Pytorch][Common] Hybrid quantization #2817".
+//
+// Single pass over x: a block is held in registers while its amax is reduced,
+// then converted with that block's scale (3 bytes of HBM traffic per element
+// plus 4 bytes per block).
+//   128 x 128: one CTA of 256 threads per block, 64 elements per thread.
+//   1 x 128:   one half-warp per tile, 8 elements per lane, four tiles in
+//              flight per half-warp; the four scales are computed one per
+//              lane and shuffled back, so each lane does one division.
+#include "fp8q_device.cuh"
+#include "fp8q_host.h"
+
+namespace fp8q {
+namespace {
+
+constexpr int kThreads = 256;
+
+// --------------------------------------------------------------- 128 x 128
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
+                float* __restrict__ scale_inv, int64_t nbc, int vec_ok) {
+    __shared__ uint32_t red[32];
+    __shared__ float s_scale;
+    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int t = threadIdx.x;
+    const bool full = vec_ok && r0 + 128 <= rows && c0 + 128 <= cols;
+
+    if (full && BF16) {
+        const int cc = t & 15, rsub = t >> 4;
+        const uint8_t* src = x + ((r0 + rsub) * cols + c0 + cc * 8) * 2;
+        uint4 v[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) v[p] = ldg_stream(src + (int64_t)p * 16 * cols * 2);
+        uint32_t m16 = 0;
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+            m16 = max_u16x2(m16, max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
+                                           max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w))));
+        const uint32_t bits = block_max_u32(fold_u16x2_to_f32bits(m16), red);
+        if (t == 0) {
+            float sc, si;  // a NaN amax (bits above Inf) gets scale 1 from the scale rule
+            scale_from_amax<FMT>(__uint_as_float(bits), 0, &sc, &si);
+            s_scale = sc;
+            scale_inv[blockIdx.y * nbc + blockIdx.x] = si;
+        }
+        __syncthreads();
+        const float scale = s_scale;
+        uint8_t* dst = q + (r0 + rsub) * cols + c0 + cc * 8;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t m;
+            Codes8 c = cvt_bf16x8<FMT>(v[p], scale, &m);
+            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[p], scale, &c);
+            stg_stream(dst + (int64_t)p * 16 * cols, make_uint2(c.lo, c.hi));
+        }
+        return;
+    }
+
+    // Guarded element path (edges, fp32 input, unaligned): two sweeps over the
+    // block, the second one re-reading x through the cache.
+    const int64_t rn = rows - r0 < 128 ? rows - r0 : 128, cn = cols - c0 < 128 ? cols - c0 : 128;
+    uint32_t am = 0;
+    for (int i = t; i < 128 * 128; i += kThreads) {
+        const int r = i >> 7, c = i & 127;
+        if (r < rn && c < cn) {
+            const int64_t e = (r0 + r) * cols + c0 + c;
+            uint32_t b = BF16 ? (uint32_t)(reinterpret_cast<const uint16_t*>(x)[e] & 0x7FFFu) << 16
+                              : (reinterpret_cast<const uint32_t*>(x)[e] & 0x7FFFFFFFu);
+            am = umax(am, b);
+        }
+    }
+    const uint32_t bits = block_max_u32(am, red);
+    if (t == 0) {
+        float sc, si;
+        scale_from_amax<FMT>(__uint_as_float(bits), 0, &sc, &si);
+        s_scale = sc;
+        scale_inv[blockIdx.y * nbc + blockIdx.x] = si;
+    }
+    __syncthreads();
+    const float scale = s_scale;
+    for (int i = t; i < 128 * 128; i += kThreads) {
+        const int r = i >> 7, c = i & 127;
+        if (r < rn && c < cn) {
+            const int64_t e = (r0 + r) * cols + c0 + c;
+            const float xv = BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16)
+                                  : reinterpret_cast<const float*>(x)[e];
+            uint32_t s;
+            q[e] = (uint8_t)quant_one<FMT>(xv, scale, &s);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ 1 x 128
+
+constexpr int kTilesInFlight = 4;  // per half-warp
+
+// Fast path: cols % 128 == 0, x and q 16-byte aligned, BF16 input; the tiles
+// are then the consecutive 128-element segments of the flat array.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+row128_bf16_kernel(const uint8_t* __restrict__ x, int64_t ntiles, uint8_t* __restrict__ q,
+                   float* __restrict__ scale_inv) {
+    const int t = threadIdx.x;
+    const int hw = t >> 4, l16 = t & 15;
+    const int lane = t & 31;
+    constexpr int kTilesPerCta = (kThreads / 16) * kTilesInFlight;
+    for (int64_t base = (int64_t)blockIdx.x * kTilesPerCta; base < ntiles; base += (int64_t)gridDim.x * kTilesPerCta) {
+        uint4 v[kTilesInFlight];
+        uint32_t amx[kTilesInFlight];
+#pragma unroll
+        for (int k = 0; k < kTilesInFlight; ++k) {
+            const int64_t tile = base + k * 16 + hw;
+            v[k] = tile < ntiles ? ldg_stream(x + tile * 256 + l16 * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kTilesInFlight; ++k) {
+            uint32_t m = max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
+                                   max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w)));
+            uint32_t b = fold_u16x2_to_f32bits(m);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) b = umax(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
+            amx[k] = b;
+        }
+        // Lane l16 < 4 of each half-warp derives the scale of tile k = l16.
+        uint32_t mine = amx[0];
+#pragma unroll
+        for (int k = 1; k < kTilesInFlight; ++k) mine = (l16 == k) ? amx[k] : mine;
+        float sc, si;
+        scale_from_amax<FMT>(__uint_as_float(mine), 0, &sc, &si);
+        if (l16 < kTilesInFlight) {
+            const int64_t tile = base + l16 * 16 + hw;
+            if (tile < ntiles) scale_inv[tile] = si;
+        }
+#pragma unroll
+        for (int k = 0; k < kTilesInFlight; ++k) {
+            const float scale = __shfl_sync(0xFFFFFFFFu, sc, (lane & 16) | k);
+            const int64_t tile = base + k * 16 + hw;
+            if (tile >= ntiles) continue;
+            uint32_t m;
+            Codes8 c = cvt_bf16x8<FMT>(v[k], scale, &m);
+            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[k], scale, &c);
+            stg_stream(q + tile * 128 + l16 * 8, make_uint2(c.lo, c.hi));
+        }
+    }
+}
+
+// Guarded path: one half-warp per (row, 128-column tile), any shape / dtype.
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+row128_guarded_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, int64_t nbc,
+                      uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    const int t = threadIdx.x, hw = t >> 4, l16 = t & 15;
+    const int64_t ntiles = rows * nbc;
+    for (int64_t tile0 = (int64_t)blockIdx.x * 16; tile0 < ntiles; tile0 += (int64_t)gridDim.x * 16) {
+        const int64_t tile = tile0 + hw;
+        const bool live = tile < ntiles;
+        const int64_t r = live ? tile / nbc : 0, j = live ? tile % nbc : 0;
+        const int64_t cbeg = j * 128, cend = cbeg + 128 < cols ? cbeg + 128 : cols;
+        uint32_t am = 0;
+        if (live)
+            for (int64_t c = cbeg + l16; c < cend; c += 16) {
+                const int64_t e = r * cols + c;
+                uint32_t b = BF16 ? (uint32_t)(reinterpret_cast<const uint16_t*>(x)[e] & 0x7FFFu) << 16
+                                  : (reinterpret_cast<const uint32_t*>(x)[e] & 0x7FFFFFFFu);
+                am = umax(am, b);
+            }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) am = umax(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+        float sc, si;
+        scale_from_amax<FMT>(__uint_as_float(am), 0, &sc, &si);
+        if (!live) continue;
+        if (l16 == 0) scale_inv[tile] = si;
+        for (int64_t c = cbeg + l16; c < cend; c += 16) {
+            const int64_t e = r * cols + c;
+            const float xv = BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16)
+                                  : reinterpret_cast<const float*>(x)[e];
+            uint32_t s;
+            q[e] = (uint8_t)quant_one<FMT>(xv, sc, &s);
+        }
+    }
+}
+
+template <int FMT>
+void launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, int br, uint8_t* q, float* si,
+                  cudaStream_t st) {
+    const int64_t nbc = (cols + 127) / 128;
+    if (br == 128) {
+        const int64_t nbr = (rows + 127) / 128;
+        const int vec_ok = aligned16(x) && aligned16(q) && cols % 16 == 0;
+        dim3 grid((unsigned)nbc, (unsigned)nbr);
+        if (bf16) block128_kernel<FMT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, q, si, nbc, vec_ok);
+        else block128_kernel<FMT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, q, si, nbc, vec_ok);
+        return;
+    }
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (bf16 && cols % 128 == 0 && aligned16(x) && aligned16(q)) {
+        const int64_t ntiles = rows * nbc;
+        constexpr int kTilesPerCta = (kThreads / 16) * kTilesInFlight;
+        int64_t grid = (ntiles + kTilesPerCta - 1) / kTilesPerCta;
+        if (grid > cap) grid = cap;
+        row128_bf16_kernel<FMT><<<(unsigned)grid, kThreads, 0, st>>>(x, ntiles, q, si);
+        return;
+    }
+    int64_t grid = (rows * nbc + 15) / 16;
+    if (grid > cap) grid = cap;
+    if (bf16) row128_guarded_kernel<FMT, true><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, nbc, q, si);
+    else row128_guarded_kernel<FMT, false><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, nbc, q, si);
+}
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols, int block_rows,
+                                           int block_cols, fp8_format_t fmt, uint8_t* q_out, float* scale_inv_out,
+                                           void* stream) {
+    const char* fn = "fp8_quantize_block";
+    if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", fn, (int)fmt);
+    if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
+    if (!((block_rows == 128 && block_cols == 128) || (block_rows == 1 && block_cols == 128)))
+        return fail(FP8_ERR_UNSUPPORTED, "%s: block shape %dx%d (supported: 128x128, 1x128)", fn, block_rows, block_cols);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (x == nullptr || q_out == nullptr || scale_inv_out == nullptr)
+        return fail(FP8_ERR_INVALID_ARG, "%s: x / q_out / scale_inv_out is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
+    if (reinterpret_cast<uintptr_t>(scale_inv_out) % 4) return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv_out not 4-byte aligned", fn);
+    if (block_rows == 128 && (rows + 127) / 128 > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: rows too large", fn);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* xp = static_cast<const uint8_t*>(x);
+    const bool bf16 = dtype == FP8_DT_BF16;
+    if (fmt == FP8_E4M3) launch_block<kE4M3>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
+    else launch_block<kE5M2>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
+    return after_launch(fn);
+}

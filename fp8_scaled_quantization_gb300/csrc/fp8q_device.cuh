@@ -1,0 +1,323 @@
+// fp8q_device.cuh -- device helpers of the sm_103a FP8 quantization kernels.
+//
+// Numerics ("Megatron FP8" §2, §4): one fp32 multiply x * scale rounded to
+// nearest-even (__fmul_rn, never contracted), then one round-to-nearest-even
+// saturating conversion to E4M3FN / E5M2 (cvt.rn.satfinite, two values per
+// instruction).  Inf / NaN inputs and the saturation count are handled off
+// the fast path: a chunk whose largest |x| bit pattern is Inf/NaN, or whose
+// largest |x| * scale exceeds FP8_MAX, is re-done element by element.  Both
+// tests are exact because fl32(|x| * s) is monotone in |x|.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp8q.h"
+
+namespace fp8q {
+
+constexpr int kE4M3 = FP8_E4M3;
+constexpr int kE5M2 = FP8_E5M2;
+
+// Largest finite magnitude of each format ("Megatron FP8" §2).
+template <int FMT> struct Fmt;
+template <> struct Fmt<kE4M3> {
+    static constexpr float kMax = 448.0f;
+    static constexpr uint32_t kMaxCode = 0x7E;  // S.1111.110
+    static constexpr uint32_t kInfCode = 0x7E;  // no Inf: +-Inf saturates
+};
+template <> struct Fmt<kE5M2> {
+    static constexpr float kMax = 57344.0f;
+    static constexpr uint32_t kMaxCode = 0x7B;  // S.11110.11
+    static constexpr uint32_t kInfCode = 0x7C;  // S.11111.00
+};
+constexpr uint32_t kNaNCode = 0x7F;
+
+// ---------------------------------------------------------------- conversions
+
+// Two fp32 -> two FP8 codes in the low 16 bits: `lo` in bits 0-7, `hi` in 8-15.
+// cvt with two f32 sources puts its first source in the upper half.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == kE4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two FP8 codes (low 16 bits of `c2`) -> two exact f16 values (f16x2).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t c2) {
+    uint32_t r;
+    if constexpr (FMT == kE4M3) {
+        uint16_t in = (uint16_t)c2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+    } else {
+        // E5M2 is the upper byte of binary16: place each code in the high byte.
+        r = __byte_perm(c2, 0u, 0x1404);  // bytes: [0, c0, 0, c1]
+    }
+    return r;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+    float f;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.f32.f16 %0, lo; }" : "=f"(f) : "r"(h2));
+    return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+    float f;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.f32.f16 %0, hi; }" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// Two fp32 -> BF16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// BF16 pair packed in a word -> fp32 (exact).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Lane-wise unsigned 16-bit maximum of two BF16 pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// |x| bit patterns of a BF16 pair; fold a u16x2 max into one fp32 bit pattern.
+__device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t fold_u16x2_to_f32bits(uint32_t m) {
+    uint32_t a = m & 0xFFFFu, b = m >> 16;
+    return (a > b ? a : b) << 16;
+}
+
+// Exact 2^k as fp32 for -126 <= k <= 127.
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// -------------------------------------------------------------- scale rule
+
+// Current scale from an amax bit pattern ("Megatron FP8" §4, §10; the
+// multiplier form FP8_MAX / amax with 2^-margin headroom).
+template <int FMT>
+__device__ __forceinline__ void scale_from_amax(float amax, int margin, float* scale, float* scale_inv) {
+    if (!(amax > 0.0f) || isinf(amax)) {
+        *scale = 1.0f;
+        *scale_inv = 1.0f;
+        return;
+    }
+    float s = __fdiv_rn(Fmt<FMT>::kMax, amax);
+    s = __fmul_rn(s, exp2i(-margin));
+    if (s > 3.402823466e+38f) s = 3.402823466e+38f;  // +Inf -> FLT_MAX
+    if (s < 1.175494351e-38f) s = 1.175494351e-38f;  // below FLT_MIN -> FLT_MIN
+    *scale = s;
+    *scale_inv = __fdiv_rn(1.0f, s);
+}
+
+__device__ __forceinline__ float scale_from_amax_rt(int fmt, float amax, int margin, float* scale_inv) {
+    float s;
+    if (fmt == kE4M3) scale_from_amax<kE4M3>(amax, margin, &s, scale_inv);
+    else scale_from_amax<kE5M2>(amax, margin, &s, scale_inv);
+    return s;
+}
+
+// ------------------------------------------------------- element-exact path
+
+// One element with every special case spelled out; used by the slow path.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant_one(float x, float scale, uint32_t* sat) {
+    uint32_t xb = __float_as_uint(x);
+    uint32_t sign = (xb >> 24) & 0x80u;
+    if (isnan(x)) { *sat = 0; return kNaNCode; }
+    if (isinf(x)) { *sat = 0; return sign | Fmt<FMT>::kInfCode; }
+    float p = __fmul_rn(x, scale);
+    *sat = fabsf(p) > Fmt<FMT>::kMax ? 1u : 0u;
+    return cvt2<FMT>(p, 0.0f) & 0xFFu;
+}
+
+// ------------------------------------------------------------ 8 BF16 -> 8 codes
+
+// Result of converting one 16-byte chunk (8 BF16) into 8 codes.
+struct Codes8 {
+    uint32_t lo, hi;  // codes 0-3, 4-7 (code i in byte i % 4)
+};
+
+// Convert 8 BF16 values (4 words) with `scale`.  `absmax` receives the u16x2
+// max of |x| over the chunk.  Special values and saturation are fixed up by
+// fixup_bf16x8 when the caller's chunk test asks for it.
+template <int FMT>
+__device__ __forceinline__ Codes8 cvt_bf16x8(uint4 v, float scale, uint32_t* absmax) {
+    Codes8 c;
+    uint32_t c0 = cvt2<FMT>(__fmul_rn(bf16lo(v.x), scale), __fmul_rn(bf16hi(v.x), scale));
+    uint32_t c1 = cvt2<FMT>(__fmul_rn(bf16lo(v.y), scale), __fmul_rn(bf16hi(v.y), scale));
+    uint32_t c2 = cvt2<FMT>(__fmul_rn(bf16lo(v.z), scale), __fmul_rn(bf16hi(v.z), scale));
+    uint32_t c3 = cvt2<FMT>(__fmul_rn(bf16lo(v.w), scale), __fmul_rn(bf16hi(v.w), scale));
+    c.lo = c0 | (c1 << 16);
+    c.hi = c2 | (c3 << 16);
+    *absmax = max_u16x2(max_u16x2(abs_bf16x2(v.x), abs_bf16x2(v.y)),
+                        max_u16x2(abs_bf16x2(v.z), abs_bf16x2(v.w)));
+    return c;
+}
+
+// True when the chunk needs the element-exact path: some |x| is Inf/NaN, or
+// (when counting saturation) the largest |x| * scale exceeds FP8_MAX.
+template <int FMT, bool COUNT_SAT>
+__device__ __forceinline__ bool chunk_needs_fixup(uint32_t absmax_f32bits, float scale) {
+    if (absmax_f32bits >= 0x7F800000u) return true;
+    if constexpr (COUNT_SAT) {
+        return __fmul_rn(__uint_as_float(absmax_f32bits), scale) > Fmt<FMT>::kMax;
+    } else {
+        return false;
+    }
+}
+
+// Redo 8 BF16 elements exactly; returns the saturated-element count.
+template <int FMT>
+__device__ __noinline__ uint32_t fixup_bf16x8(uint4 v, float scale, Codes8* c) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2] = {0u, 0u};
+    uint32_t sat = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float x = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+        uint32_t s;
+        uint32_t code = quant_one<FMT>(x, scale, &s);
+        sat += s;
+        out[i >> 2] |= code << (8 * (i & 3));
+    }
+    c->lo = out[0];
+    c->hi = out[1];
+    return sat;
+}
+
+// ----------------------------------------------------------- fp32 inputs
+
+// Convert 4 fp32 values into 4 codes (one word).
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_f32x4(float4 v, float scale, uint32_t* absmax) {
+    uint32_t c0 = cvt2<FMT>(__fmul_rn(v.x, scale), __fmul_rn(v.y, scale));
+    uint32_t c1 = cvt2<FMT>(__fmul_rn(v.z, scale), __fmul_rn(v.w, scale));
+    uint32_t a = __float_as_uint(v.x) & 0x7FFFFFFFu, b = __float_as_uint(v.y) & 0x7FFFFFFFu;
+    uint32_t c = __float_as_uint(v.z) & 0x7FFFFFFFu, d = __float_as_uint(v.w) & 0x7FFFFFFFu;
+    *absmax = umax(umax(a, b), umax(c, d));
+    return c0 | (c1 << 16);
+}
+
+template <int FMT>
+__device__ __noinline__ uint32_t fixup_f32x4(float4 v, float scale, uint32_t* code4) {
+    float e[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0, sat = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t s;
+        out |= quant_one<FMT>(e[i], scale, &s) << (8 * i);
+        sat += s;
+    }
+    *code4 = out;
+    return sat;
+}
+
+// ----------------------------------------------------------- reductions
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(0xFFFFFFFFu, v); }
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) { return __reduce_add_sync(0xFFFFFFFFu, v); }
+
+// Block-wide max / sum for blockDim.x a multiple of 32 (<= 1024).  `smem`
+// holds 32 words; the result is valid in every thread.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* smem) {
+    v = warp_max_u32(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    v = lane < nw ? smem[lane] : 0u;
+    return warp_max_u32(v);
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* smem) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    __syncthreads();
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    v = lane < nw ? smem[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ------------------------------------------------ single-launch grid finish
+
+// Per-(device, stream) workspace; every launch that uses it leaves it zero.
+struct alignas(64) Workspace {
+    unsigned int done;            // CTAs finished in the current launch
+    unsigned int amax_bits;       // running max of |x| as fp32 bits
+    unsigned long long sat;       // running saturated-element count
+    unsigned int pad[12];
+};
+static_assert(sizeof(Workspace) == 64, "workspace is one 64-byte line");
+
+// What the last CTA of a launch writes.
+struct FinishArgs {
+    float* amax_out;                     // nullable
+    float* scale_out;                    // nullable
+    float* scale_inv_out;                // nullable
+    unsigned long long* sat_out;         // nullable
+    int fmt;
+    int margin;
+};
+
+// Fold this CTA's amax / saturation count into the workspace; the last CTA
+// reads the totals, resets the workspace and writes the outputs.  Called by
+// every thread of every CTA with the CTA-reduced values valid in thread 0.
+// Never waits: the last CTA is the one whose arrival completes the count.
+__device__ __forceinline__ void grid_finish(Workspace* ws, uint32_t cta_amax_bits,
+                                            unsigned long long cta_sat, const FinishArgs& fa) {
+    if (threadIdx.x != 0) return;
+    if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
+    if (cta_sat) atomicAdd(&ws->sat, cta_sat);
+    __threadfence();
+    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned int prev = atomicAdd(&ws->done, 1u);
+    if (prev != total - 1) return;
+    __threadfence();
+    uint32_t bits = atomicExch(&ws->amax_bits, 0u);
+    unsigned long long sat = atomicExch(&ws->sat, 0ull);
+    atomicExch(&ws->done, 0u);
+    if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
+    const float amax = __uint_as_float(bits);
+    if (fa.amax_out) *fa.amax_out = amax;
+    if (fa.sat_out) *fa.sat_out = sat;
+    if (fa.scale_out) {
+        float si;
+        float s = scale_from_amax_rt(fa.fmt, amax, fa.margin, &si);
+        *fa.scale_out = s;
+        *fa.scale_inv_out = si;
+    }
+}
+
+// ------------------------------------------------------------ memory ops
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+}  // namespace fp8q

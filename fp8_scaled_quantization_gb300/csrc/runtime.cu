@@ -1,0 +1,112 @@
+// runtime.cu -- status strings, per-thread error text, launch counting, SM
+// count cache and the per-(device, stream) reduction workspace.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "fp8q_device.cuh"
+#include "fp8q_host.h"
+
+namespace fp8q {
+
+namespace {
+thread_local char g_last_error[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+
+std::mutex g_mu;
+std::map<int, int> g_sm_count;                                 // device -> SMs
+std::map<std::pair<int, uintptr_t>, Workspace*> g_workspaces;  // (device, stream) -> ws
+}  // namespace
+
+fp8_status_t fail(fp8_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fp8_status_t cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return FP8_OK;
+    return fail(FP8_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+fp8_status_t after_launch(const char* kernel) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e, kernel);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return FP8_OK;
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sm_count.find(dev);
+    if (it != g_sm_count.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sm_count[dev] = n;
+    return n;
+}
+
+Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st) {
+    *st = FP8_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_status(e, "cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+    auto it = g_workspaces.find(key);
+    if (it != g_workspaces.end()) return it->second;
+    // First use on this stream.  Relax the thread's capture mode so that the
+    // allocation is legal while a stream is being captured; the zeroing is
+    // enqueued on the stream itself, so under capture it becomes a graph node
+    // ordered before the kernel that needs it.
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    void* p = nullptr;
+    e = cudaMalloc(&p, sizeof(Workspace));
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+        *st = cuda_status(e, "cudaMalloc(workspace)");
+        return nullptr;
+    }
+    e = cudaMemsetAsync(p, 0, sizeof(Workspace), stream);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        *st = cuda_status(e, "cudaMemsetAsync(workspace)");
+        return nullptr;
+    }
+    auto* ws = static_cast<Workspace*>(p);
+    g_workspaces[key] = ws;
+    return ws;
+}
+
+}  // namespace fp8q
+
+extern "C" {
+
+const char* fp8_status_string(fp8_status_t status) {
+    switch (status) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG";
+        case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
+    }
+    return "FP8_ERR_UNKNOWN";
+}
+
+const char* fp8_last_error_message(void) { return fp8q::g_last_error; }
+
+int fp8_version(void) { return (FP8Q_VERSION_MAJOR << 16) | FP8Q_VERSION_MINOR; }
+
+unsigned long long fp8_launch_count(void) { return fp8q::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

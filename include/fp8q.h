@@ -1,0 +1,244 @@
+/*
+ * fp8q.h -- C ABI of the GB300 (sm_103a) FP8 scaled-quantization library.
+ *
+ * The library computes the data-parallel hot path of FP8 tensor
+ * quantization with scaling:
+ *   amax reduction -> scale (current, or delayed from an amax history)
+ *   -> round-to-nearest-even saturating cast of BF16/FP32 to E4M3FN or E5M2
+ *   (rowwise, columnwise/transposed, 128x128 and 1x128 block-scaled)
+ *   -> dequantize.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every tensor and scalar pointer is a DEVICE pointer owned by the
+ *           caller (for example a PyTorch allocation).  The library never
+ *           frees caller memory and never synchronises the device or a stream.
+ *           The one allocation it makes is a 64-byte reduction workspace per
+ *           (device, stream) pair, created on the first call that needs it
+ *           and kept until process exit (see "Workspace" below).
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *           default stream.  Every call only enqueues work on that stream and
+ *           returns; results are ready when the stream reaches them.
+ * Layout.   Row-major and contiguous.  BF16 is the 16-bit brain-float bit
+ *           pattern; FP8 codes are bytes (E4M3FN or E5M2 encodings).
+ * Scale.    The multiplier convention: q = encode(fl32(x * scale)),
+ *           x ~= decode(q) * scale_inv, scale_inv = fl32(1 / scale).
+ * Errors.   Arguments are checked on the host before anything is enqueued; a
+ *           rejected call returns FP8_ERR_INVALID_ARG / FP8_ERR_UNSUPPORTED
+ *           and touches no memory.  FP8_ERR_CUDA is returned when a CUDA
+ *           runtime call or kernel launch fails; fp8_last_error_message()
+ *           gives the text.  Kernels never trap or assert on the device.
+ * Counters. Outputs named *_out (amax, saturation count, scales) are
+ *           overwritten, never accumulated into.
+ * Workspace. Reductions that finish in a single launch (amax with a fused
+ *           scale, fused amax / saturation count) use a 64-byte per-(device,
+ *           stream) workspace that every launch leaves zeroed.  Calls on the
+ *           same stream are ordered and safe.  Calls on different streams use
+ *           different workspaces and are safe.  A CUDA graph captured from a
+ *           stream keeps that stream's workspace address: do not replay such a
+ *           graph concurrently with other work on the capturing stream.  The
+ *           first call on a new stream allocates (cudaMalloc) with the
+ *           thread's capture mode relaxed, so it may happen during capture.
+ *
+ * Special values (the same in every cast):
+ *   x NaN          -> code 0x7F (canonical NaN, sign dropped)
+ *   x +-Inf        -> E5M2: +-Inf (0x7C / 0xFC); E4M3FN: +-448 (0x7E / 0xFE)
+ *   x finite       -> fl32(x * scale) rounded to nearest-even onto the FP8
+ *                     grid; magnitudes at or beyond the largest finite value
+ *                     (448 / 57344) saturate to it; signed zeros keep sign.
+ *
+ * Scale rule (current and delayed):
+ *   amax == 0, negative, NaN or Inf -> scale = scale_inv = 1
+ *   else scale = fl32(fl32(FP8_MAX / amax) * 2^-margin), clamped to
+ *        [FLT_MIN, FLT_MAX]; scale_inv = fl32(1 / scale).
+ *
+ * Page citations use the page title and section: "Megatron FP8" (a Megatron
+ * / Transformer Engine FP8 training guide, sections §2 .. §28), "Low
+ * Precision Training and Rollout" (vime documentation), "[Pytorch][Common]
+ * Hybrid quantization #2817" (a Transformer Engine pull request).
+ */
+#ifndef FP8Q_H_
+#define FP8Q_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8Q_VERSION_MAJOR 0
+#define FP8Q_VERSION_MINOR 1
+
+/* "Megatron FP8" §2: E4M3 here is E4M3FN (bias 7, max 448, no Inf, NaN only
+ * at S.1111.111); E5M2 is IEEE-like (bias 15, max 57344, Inf and NaN). */
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
+
+/* Element type of high-precision tensors. */
+typedef enum { FP8_DT_BF16 = 0, FP8_DT_FP32 = 1 } fp8_dtype_t;
+
+/* "Megatron FP8" §5 / §7: amax_compute_algo of the delayed recipe. */
+typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad enum or margin */
+    FP8_ERR_UNSUPPORTED = 2, /* e.g. block shape other than 128x128 / 1x128     */
+    FP8_ERR_CUDA = 3         /* a CUDA runtime call or launch failed            */
+} fp8_status_t;
+
+/* Static text for a status code. */
+const char* fp8_status_string(fp8_status_t status);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char* fp8_last_error_message(void);
+
+/* Library version as (major << 16) | minor. */
+int fp8_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads).  Lets a caller count launches inside a timed region. */
+unsigned long long fp8_launch_count(void);
+
+/* ------------------------------------------------------------------------ */
+/* amax reduction with optional fused current-scaling finalize              */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §4 (amax = max|x| by a dedicated reduction kernel, stored
+ * as an fp32 scalar; scale_inv cached) and §10 (current scaling: scan the
+ * tensor before the cast; margin headroom).
+ *
+ *   x           device, n elements of `dtype`, any alignment.
+ *   n           element count, >= 0 (n == 0: amax 0, scale 1).
+ *   amax_out    device float[1]: max_i |x_i|; NaN if any x_i is NaN
+ *               (written as 0x7FC00000).
+ *   fmt, margin used only when scale_out is given; -126 <= margin <= 126.
+ *   scale_out, scale_inv_out
+ *               device float[1] each, both NULL or both set: the current
+ *               scale from this amax (scale rule above), computed in the same
+ *               launch by the last CTA to finish.
+ * One kernel launch. */
+fp8_status_t fp8_amax(const void* x, fp8_dtype_t dtype, int64_t n, float* amax_out,
+                      fp8_format_t fmt, int margin, float* scale_out, float* scale_inv_out,
+                      void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Delayed scaling: amax-history update and scale                           */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §5 (amax history ring buffer; the slot step % history_len
+ * takes the newest amax; eff = window max for algo max, the slot just
+ * written for most_recent; scale 1 while the history is all zero) and §7
+ * (amax_history_len, amax_compute_algo, margin).
+ *
+ *   amax_history  device float[history_len], caller-owned and caller
+ *                 zero-initialised; updated in place.
+ *   history_len   1 .. 65536.
+ *   step          >= 0; the slot written is step % history_len.
+ *   new_amax      device float[1] or NULL.  When set, it is stored into the
+ *                 slot before the maximum is taken (typically the amax that
+ *                 fp8_quantize recorded for the tensor of this step).
+ *   algo, fmt, margin   as above.
+ *   scale_out, scale_inv_out  device float[1] each (required): the scale for
+ *                 the NEXT cast.
+ * Per step k of the delayed recipe: fp8_quantize(x_k, scale) records amax_k,
+ * then fp8_update_scale_delayed(.., step = k, new_amax = amax_k, ..) gives
+ * the scale of step k + 1.  Before step 0, a call with new_amax = NULL on the
+ * zero history gives scale 1.  history_len 1 with most_recent equals current
+ * scaling.  One single-CTA launch. */
+fp8_status_t fp8_update_scale_delayed(float* amax_history, int history_len, int64_t step,
+                                      const float* new_amax, fp8_amax_algo_t algo,
+                                      fp8_format_t fmt, int margin, float* scale_out,
+                                      float* scale_inv_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Per-tensor quantize                                                       */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §4 (x scaled, clamped to +-FP8_MAX), §2 (E4M3FN saturates,
+ * E5M2 keeps Inf), §6 (cast_to_fp8 before the FP8 GEMM), §24 (per-layer
+ * overflow counts).
+ *
+ *   x              device, n elements of `dtype`, any alignment (16-byte
+ *                  aligned x and q_out take the vector path).
+ *   n              >= 0.
+ *   scale          device float[1]: the multiplier.
+ *   q_out          device uint8[n]: the codes.
+ *   amax_out       device float[1] or NULL: max|x| of this tensor, fused
+ *                  (the delayed recipe records it for the next update).
+ *   sat_count_out  device uint64[1] or NULL: number of finite x_i with
+ *                  |fl32(x_i * scale)| > FP8_MAX.
+ * One kernel launch. */
+fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
+                          const float* scale, uint8_t* q_out, float* amax_out,
+                          unsigned long long* sat_count_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Quantize with rowwise + columnwise (transposed) outputs                  */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §6 (the weight-gradient GEMM consumes transpose(dy_fp8)) and
+ * the columnwise storage of "[Pytorch][Common] Hybrid quantization #2817"
+ * (a physically transposed FP8 copy for Hopper-style GEMMs;
+ * columnwise_source = original).  Both copies use the one scale, so
+ * q_col[c, r] == q_row[r, c] bit for bit.
+ *
+ *   x        device [rows, cols] of `dtype`, row-major.
+ *   rows, cols  >= 0.
+ *   scale    device float[1].
+ *   q_row    device uint8[rows, cols] or NULL (columnwise only).
+ *   q_col    device uint8[cols, rows] or NULL (rowwise only); not both NULL.
+ *   amax_out device float[1] or NULL: max|x|, fused.
+ * Current scaling is fp8_amax(.., scale_out, scale_inv_out) followed by this
+ * call.  Interior 128x128 tiles take the vector path when cols % 16 == 0,
+ * rows % 16 == 0 and the pointers are 16-byte aligned; edge tiles and other
+ * shapes take a guarded element path.  One kernel launch. */
+fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64_t rows,
+                                         int64_t cols, fp8_format_t fmt, const float* scale,
+                                         uint8_t* q_row, uint8_t* q_col, float* amax_out,
+                                         void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Block-scaled quantize (128x128 and 1x128)                                 */
+/* ------------------------------------------------------------------------ */
+/* "Low Precision Training and Rollout": block FP8 with 128x128 blocks
+ * ("BF16 Training with FP8 Rollout", --block-size 128 128), FP32 block scales
+ * ("FP8 Quick Start", NVTE_FP8_BLOCK_SCALING_FP32_SCALES=1), the stored block
+ * factor being the inverse scale ("MXFP8 (Blackwell only)": weight_scale_inv);
+ * the 1x128 tile is the activation-side Float8Blockwise shape named in
+ * "[Pytorch][Common] Hybrid quantization #2817".
+ *
+ * For every block: amax over its elements (edge blocks: the elements that
+ * exist), scale by the scale rule with margin 0, codes with that scale.
+ *
+ *   x              device [rows, cols] of `dtype`, row-major.
+ *   block_rows, block_cols   (128, 128) or (1, 128); else FP8_ERR_UNSUPPORTED.
+ *   q_out          device uint8[rows, cols].
+ *   scale_inv_out  device float[ceil(rows/block_rows), ceil(cols/block_cols)],
+ *                  row-major: the dequantization multiplier of each block.
+ * One kernel launch. */
+fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
+                                int block_rows, int block_cols, fp8_format_t fmt, uint8_t* q_out,
+                                float* scale_inv_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dequantize                                                                */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §4 (scale_inv cached so dequantize is one multiply) and §23
+ * (reconstructed = fp8 value * scale); "Low Precision Training and Rollout",
+ * "Implementation Notes" (FP8 weights dequantized to BF16).
+ *
+ * y = decode(q) * scale_inv in fp32 (one multiply), then rounded to nearest
+ * even into BF16 (out_dtype FP8_DT_BF16) or kept as fp32 (FP8_DT_FP32).
+ * NaN results are written as the canonical NaN (BF16 0x7FFF, fp32 0x7FFFFFFF).
+ *
+ *   q          device uint8[rows, cols].
+ *   scale_inv  device float: one value when block_rows = block_cols = 0
+ *              (per-tensor), else the [ceil(rows/br), ceil(cols/bc)] block
+ *              grid of fp8_quantize_block with (br, bc) = (128,128) or (1,128).
+ *   y          device [rows, cols] of out_dtype.
+ * One kernel launch. */
+fp8_status_t fp8_dequantize(const uint8_t* q, fp8_format_t fmt, int64_t rows, int64_t cols,
+                            const float* scale_inv, int block_rows, int block_cols, void* y,
+                            fp8_dtype_t out_dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H_ */

@@ -1,0 +1,171 @@
+"""Host-side logic that needs no GPU: the C ABI library loads and exports every
+entry point its header declares, argument validation rejects bad calls
+before touching a device, the byte accounting of the benchmark, the
+multi-rank reduction over gloo, and the reference arm's JSON line."""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+import fp8_scaled_quantization_gb300 as fq
+from fp8_scaled_quantization_gb300 import _lib
+from conftest import ROOT
+
+
+def test_library_exports_every_header_symbol(native_lib):
+    names = _lib.header_entry_points()
+    assert {"fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
+            "fp8_quantize_block", "fp8_dequantize"} <= set(names)
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) <= set(_lib.SIGNATURES), "every declared entry point has a binding signature"
+
+
+def test_library_built_for_sm103a(native_lib):
+    from fp8_scaled_quantization_gb300 import build as b
+    assert "arch=compute_103a,code=sm_103a" in b.ARCH
+    assert "-ffast-math" not in b.NVCC_FLAGS and "--use_fast_math" not in b.NVCC_FLAGS
+
+
+def test_status_strings_and_version(native_lib):
+    assert native_lib.fp8_status_string(0) == b"FP8_OK"
+    assert native_lib.fp8_status_string(2) == b"FP8_ERR_UNSUPPORTED"
+    assert native_lib.fp8_version() == (0 << 16) | 1
+
+
+BAD = 0x1000  # never dereferenced: every call below is rejected on the host first
+
+
+@pytest.mark.parametrize("call,status,msg", [
+    (lambda L: L.fp8_quantize(BAD, 0, 10, 9, BAD, BAD, None, None, None), 1, "unknown format"),
+    (lambda L: L.fp8_quantize(BAD, 5, 10, 0, BAD, BAD, None, None, None), 1, "unknown dtype"),
+    (lambda L: L.fp8_quantize(BAD, 0, -1, 0, BAD, BAD, None, None, None), 1, "n < 0"),
+    (lambda L: L.fp8_quantize(BAD, 0, 10, 0, None, BAD, None, None, None), 1, "scale is NULL"),
+    (lambda L: L.fp8_quantize(BAD + 1, 0, 10, 0, BAD, BAD, None, None, None), 1, "element-aligned"),
+    (lambda L: L.fp8_amax(BAD, 0, 10, None, 0, 0, None, None, None), 1, "amax_out is NULL"),
+    (lambda L: L.fp8_amax(BAD, 0, 10, BAD, 0, 0, BAD, None, None), 1, "both"),
+    (lambda L: L.fp8_amax(BAD, 0, 10, BAD, 0, 127, BAD, BAD, None), 1, "margin"),
+    (lambda L: L.fp8_update_scale_delayed(BAD, 0, 0, None, 0, 0, 0, BAD, BAD, None), 1, "history_len"),
+    (lambda L: L.fp8_update_scale_delayed(BAD, 4, -1, None, 0, 0, 0, BAD, BAD, None), 1, "step < 0"),
+    (lambda L: L.fp8_update_scale_delayed(BAD, 4, 0, None, 3, 0, 0, BAD, BAD, None), 1, "unknown algo"),
+    (lambda L: L.fp8_update_scale_delayed(BAD, 4, 0, None, 0, 0, 0, None, BAD, None), 1, "NULL"),
+    (lambda L: L.fp8_quantize_cast_transpose(BAD, 0, 4, 4, 0, BAD, None, None, None, None), 1, "both NULL"),
+    (lambda L: L.fp8_quantize_cast_transpose(BAD, 0, -4, 4, 0, BAD, BAD, None, None, None), 1, "negative"),
+    (lambda L: L.fp8_quantize_block(BAD, 0, 4, 4, 64, 64, 0, BAD, BAD, None), 2, "block shape"),
+    (lambda L: L.fp8_quantize_block(BAD, 0, 4, 4, 128, 1, 0, BAD, BAD, None), 2, "block shape"),
+    (lambda L: L.fp8_quantize_block(BAD, 0, 4, 4, 128, 128, 0, None, BAD, None), 1, "NULL"),
+    (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 32, 32, BAD, 0, None), 2, "block shape"),
+    (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 0, 0, BAD, 7, None), 1, "out_dtype"),
+    (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD + 2, 0, 0, BAD, 0, None), 1, "scale_inv not 4-byte"),
+])
+def test_host_validation_rejects_before_launch(native_lib, call, status, msg):
+    before = native_lib.fp8_launch_count()
+    assert call(native_lib) == status
+    assert msg in native_lib.fp8_last_error_message().decode()
+    assert native_lib.fp8_launch_count() == before
+
+
+def test_empty_inputs_need_no_device(native_lib):
+    # nothing to do and no reduction requested: success without touching CUDA
+    assert native_lib.fp8_quantize(None, 0, 0, 0, BAD, None, None, None, None) == 0
+    assert native_lib.fp8_quantize_block(None, 0, 0, 128, 128, 128, 0, None, None, None) == 0
+    assert native_lib.fp8_dequantize(None, 0, 0, 5, None, 0, 0, None, 0, None) == 0
+
+
+def test_binding_rejects_host_and_strided_tensors(native_lib):
+    x = torch.zeros(16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fq.fp8_quantize(x, fq.E4M3, torch.ones(1), torch.empty(16, dtype=torch.uint8))
+    with pytest.raises(TypeError):
+        fq.fp8_quantize(x, fq.E4M3, torch.ones(1), torch.empty(16, dtype=torch.int8))
+
+
+def test_library_missing_fails_loudly(tmp_path):
+    with pytest.raises(_lib.LibraryMissing):
+        saved = _lib._lib
+        try:
+            _lib._lib = None
+            _lib.load(str(tmp_path / "nope.so"))
+        finally:
+            _lib._lib = saved
+
+
+# ------------------------------------------------------------ byte accounting
+
+def test_pipeline_byte_accounting_full_size():
+    import bench
+    from fp8_scaled_quantization_gb300 import pipelines as P
+    shapes = bench.workload_shapes(1.0)
+    meta = torch.device("meta")
+    mk = lambda s: torch.empty(s, dtype=torch.bfloat16, device=meta)  # noqa: E731
+    inp = {"w1": mk(shapes["w1"]), "w2": mk(shapes["w2"]), "w3": [mk(shapes["w3"]) for _ in range(16)],
+           "w4": (mk(shapes["w4w"]), mk(shapes["w4a"])), "w5": [mk(shapes["w5"]) for _ in range(32)]}
+    pipes = bench.make_pipelines(inp)
+    b = {k: p.bytes() for k, p in pipes.items()}
+    N1, N2, N3, N5 = 1024 * 1024, 8192 * 8192, 4096 * 14336, 8192 * 8192
+    assert b["W1"].total == 5 * N1
+    assert b["W2"].total == 6 * N2
+    assert b["W3"].per_kernel["quantize"] == (16 * 3 * N3, 16)
+    assert b["W4"].per_kernel["block128x128"][0] == 3 * 7168 * 18432 + 4 * 56 * 144
+    assert b["W4"].per_kernel["block1x128"][0] == 3 * 16384 * 7168 + 4 * 16384 * 56
+    assert b["W5"].total == 32 * 8 * N5
+    total = sum(x.total for x in b.values())
+    assert 21.0e9 < total < 21.3e9
+    assert sum(x.launches for x in b.values()) == 2 + 2 + (16 + 17) + 2 + 96
+
+
+# ------------------------------------------------------------- multi-rank
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.max_over_ranks(10.0 + 5 * rank, world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    import socket
+    import torch.multiprocessing as mp
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert got == [(0, 15.0), (1, 15.0)]
+
+
+def test_reference_arm_line_shape():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--scale", "0.125"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_nonzero_rank_exits_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
