@@ -45,21 +45,25 @@ WORKLOAD_NAME = ("fp8 scaled-quantization suite: W1 current E4M3 1024x1024; W2 c
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="shrink every workload's row count by this factor (testing only; 1.0 = full size)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-fraction", type=float, default=1.0 / 16,
+    ap.add_argument("--cpu-fraction", type=float, default=1.0 / 4,
                     help="fraction of each workload the CPU-oracle baseline processes")
+    ap.add_argument("--workloads", default="W1,W2,W3,W4,W5",
+                    help="comma-separated subset of W1..W5 (profiling a single workload)")
+    ap.add_argument("--count", type=int, default=0,
+                    help="cap on W3 steps and W5 tensors (0 = the full 16 / 32; profiling only)")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------- workloads
 
-def workload_shapes(scale: float):
+def workload_shapes(scale: float, count: int = 0):
     from fp8_scaled_quantization_gb300 import workloads as wl
 
     def s(shape, mult=128):
@@ -73,31 +77,45 @@ def workload_shapes(scale: float):
         "w4w": s(wl.W4_WEIGHT_SHAPE),
         "w4a": s(wl.W4_ACT_SHAPE),
         "w5": s(wl.W5_SHAPE),
-        "w3_steps": wl.W3_STEPS,
-        "w5_count": wl.W5_TENSORS,
+        "w3_steps": min(wl.W3_STEPS, count) if count > 0 else wl.W3_STEPS,
+        "w5_count": min(wl.W5_TENSORS, count) if count > 0 else wl.W5_TENSORS,
     }
 
 
-def make_inputs(shapes, device, seed_offset=0):
+ALL_WORKLOADS = ("W1", "W2", "W3", "W4", "W5")
+
+
+def make_inputs(shapes, device, seed_offset=0, which=ALL_WORKLOADS):
     from fp8_scaled_quantization_gb300 import workloads as wl
     S = wl.SEEDS
-    x1 = wl.w1_outliers(shapes["w1"], device, seed=S["w1"] + seed_offset)
-    x2 = wl.w2_student_t(shapes["w2"], device, seed=S["w2"] + seed_offset)
-    x3 = list(wl.w3_steps(shapes["w3"], shapes["w3_steps"], device, seed=S["w3"] + seed_offset))
-    w4, a4 = wl.w4_block(shapes["w4w"], shapes["w4a"], device, seed=S["w4"] + seed_offset)
-    x5 = list(wl.w5_gradients(shapes["w5"], shapes["w5_count"], device, seed=S["w5"] + seed_offset))
-    return {"w1": x1, "w2": x2, "w3": x3, "w4": (w4, a4), "w5": x5}
+    inp = {}
+    if "W1" in which:
+        inp["w1"] = wl.w1_outliers(shapes["w1"], device, seed=S["w1"] + seed_offset)
+    if "W2" in which:
+        inp["w2"] = wl.w2_student_t(shapes["w2"], device, seed=S["w2"] + seed_offset)
+    if "W3" in which:
+        inp["w3"] = list(wl.w3_steps(shapes["w3"], shapes["w3_steps"], device, seed=S["w3"] + seed_offset))
+    if "W4" in which:
+        inp["w4"] = wl.w4_block(shapes["w4w"], shapes["w4a"], device, seed=S["w4"] + seed_offset)
+    if "W5" in which:
+        inp["w5"] = list(wl.w5_gradients(shapes["w5"], shapes["w5_count"], device, seed=S["w5"] + seed_offset))
+    return inp
 
 
 def make_pipelines(inp):
     from fp8_scaled_quantization_gb300 import pipelines as P, E4M3, E5M2
-    return {
-        "W1": P.CurrentScaling(inp["w1"], E4M3, 0),
-        "W2": P.CurrentCastTranspose(inp["w2"], E4M3, 1),
-        "W3": P.DelayedScaling(inp["w3"], 1024, E4M3, 0),
-        "W4": P.BlockScaling(*inp["w4"], E4M3),
-        "W5": P.GradientQDQ(inp["w5"], E5M2, 0),
-    }
+    pipes = {}
+    if "w1" in inp:
+        pipes["W1"] = P.CurrentScaling(inp["w1"], E4M3, 0)
+    if "w2" in inp:
+        pipes["W2"] = P.CurrentCastTranspose(inp["w2"], E4M3, 1)
+    if "w3" in inp:
+        pipes["W3"] = P.DelayedScaling(inp["w3"], 1024, E4M3, 0)
+    if "w4" in inp:
+        pipes["W4"] = P.BlockScaling(*inp["w4"], E4M3)
+    if "w5" in inp:
+        pipes["W5"] = P.GradientQDQ(inp["w5"], E5M2, 0)
+    return pipes
 
 
 # --------------------------------------------------------------------- timing
@@ -217,6 +235,24 @@ def kernel_traffic(kernel: str):
 
 # ------------------------------------------------------------------ our arm
 
+def compulsory_bytes(pipes) -> int:
+    """Bytes each workload must move at least: its inputs read once and its
+    outputs written once (amax passes and re-reads not counted)."""
+    total = 0
+    for name, p in pipes.items():
+        if name == "W1":
+            total += p.x.numel() * (p.x.element_size() + 1)
+        elif name == "W2":
+            total += p.x.numel() * (p.x.element_size() + 2)
+        elif name == "W3":
+            total += sum(x.numel() * (x.element_size() + 1) for x in p.xs)
+        elif name == "W4":
+            total += p.bytes().total
+        elif name == "W5":
+            total += sum(x.numel() * (x.element_size() + 1 + 1 + 2) for x in p.xs)
+    return total
+
+
 def run_ours(args, rank, world):
     import torch
     import fp8_scaled_quantization_gb300 as fq
@@ -225,15 +261,18 @@ def run_ours(args, rank, world):
     fq.library()  # raises if the CUDA library is missing: there is no fallback
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    shapes = workload_shapes(args.scale)
-    inp = make_inputs(shapes, dev, seed_offset=rank)
+    shapes = workload_shapes(args.scale, args.count)
+    which = tuple(w.strip().upper() for w in args.workloads.split(",") if w.strip())
+    full_suite = set(which) == set(ALL_WORKLOADS) and args.scale == 1.0 and args.count == 0
+    inp = make_inputs(shapes, dev, seed_offset=rank, which=which)
     pipes = make_pipelines(inp)
     per_variant_bytes = {k: p.bytes() for k, p in pipes.items()}
     kb = KernelBytes()
     for b in per_variant_bytes.values():
         for name, (nbytes, launches) in b.per_kernel.items():
             kb.add(name, nbytes // launches, launches)
-    step_bytes = kb.total
+    kernel_bytes = kb.total
+    step_bytes = compulsory_bytes(pipes)
     torch.cuda.synchronize()
 
     def step(timer=None, vt=None):
@@ -253,7 +292,8 @@ def run_ours(args, rank, world):
     vtimer.reserve(2 * len(pipes) * args.steps + 8)
     gpu_uuid = None
     try:
-        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
     except Exception:
         pass
     clocks = ClockSampler(gpu_uuid)
@@ -280,52 +320,62 @@ def run_ours(args, rank, world):
     kernels = {}
     for name, (tot_ms, n) in timer.totals().items():
         nbytes, nl = kb.per_kernel[name]
-        nbytes_run = nbytes * args.steps
-        gbs = nbytes_run / (tot_ms * 1e-3) / 1e9
-        kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": tot_ms / args.steps,
-                         "avg_launch_us": tot_ms * 1e3 / n, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        gbs = nbytes * args.steps / (tot_ms * 1e-3) / 1e9
+        kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": round(tot_ms / args.steps, 4),
+                         "avg_launch_us": round(tot_ms * 1e3 / n, 2), "gbs": round(gbs, 1),
+                         "frac": round(gbs / peak, 4)}
     dominant = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
     dk = kernels[dominant]
     variants = {}
     for name, (tot_ms, n) in vtimer.totals().items():
-        b = per_variant_bytes[name].total
-        gbs = b * args.steps / (tot_ms * 1e-3) / 1e9
-        variants[name] = {"bytes_per_step": b, "ms_per_step": round(tot_ms / args.steps, 4), "gbs": round(gbs, 1),
+        cb = compulsory_bytes({name: pipes[name]})
+        gbs = cb * args.steps / (tot_ms * 1e-3) / 1e9
+        variants[name] = {"compulsory_bytes": cb, "kernel_bytes": per_variant_bytes[name].total,
+                          "ms_per_step": round(tot_ms / args.steps, 4), "gbs": round(gbs, 1),
                           "frac": round(gbs / peak, 4)}
     traffic_per_elem = kernel_traffic(dominant)
-    elems_per_launch = None
-    if traffic_per_elem is not None:
-        per_elem_bytes = {"quantize": 3, "cast_transpose": 4, "amax": 2, "dequantize": 3}.get(dominant)
-        if per_elem_bytes:
-            elems_per_launch = dk["bytes_per_step"] / dk["launches_per_step"] / per_elem_bytes
+    per_elem_bytes = {"quantize": 3, "cast_transpose": 4, "amax": 2, "dequantize": 3}.get(dominant)
+    alg_per_launch = dk["bytes_per_step"] / dk["launches_per_step"]
+    traffic = None
+    if traffic_per_elem is not None and per_elem_bytes:
+        traffic = round(traffic_per_elem * alg_per_launch / per_elem_bytes)
     value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "io": "bf16 in, e4m3/e5m2 uint8 codes out (W5: bf16 out)",
-                   "bytes_per_step": step_bytes, "row_scale": args.scale,
-                   "l2": "no flush: inputs (%.1f GB) and per-step traffic (%.1f GB) exceed the 126 MB L2"
-                         % (sum(t.numel() * t.element_size() for t in _all_inputs(inp)) / 1e9, step_bytes / 1e9),
+        "config": {"workload": WORKLOAD_NAME if full_suite else f"subset {','.join(which)} scale {args.scale} "
+                                                                f"count {args.count or 'full'}",
+                   "io": "bf16 in, e4m3/e5m2 uint8 codes out (W5: bf16 out)",
+                   "bytes": "compulsory: each workload's inputs read once + outputs written once",
+                   "compulsory_bytes_per_step": step_bytes, "kernel_bytes_per_step": kernel_bytes,
+                   "kernel_gbs": round(world * kernel_bytes * args.steps / (ms_max * 1e-3) / 1e9, 1),
+                   "l2": "no flush: inputs (%.2f GB) and per-step traffic (%.2f GB) exceed the 126 MB L2"
+                         % (sum(t.numel() * t.element_size() for t in _all_inputs(inp)) / 1e9, kernel_bytes / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
                      "frac": round(dk["gbs"] / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": (round(traffic_per_elem * elems_per_launch) if elems_per_launch else None),
-                     "algorithmic_bytes_per_launch": round(dk["bytes_per_step"] / dk["launches_per_step"])},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": round(alg_per_launch)},
         "kernels": kernels,
         "variants": variants,
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if not args.no_e2e:
+    if not args.no_e2e and full_suite:
         result["e2e"] = run_e2e(args, pipes, inp, step_bytes, world)
-    if not args.no_cpu_baseline and rank == 0 and world == 1:
+    if not args.no_cpu_baseline and rank == 0 and world == 1 and full_suite:
         result["cpu_baseline"] = cpu_baseline(args, inp)
     return result
 
 
 def _all_inputs(inp):
-    out = [inp["w1"], inp["w2"], *inp["w3"], *inp["w4"], *inp["w5"]]
+    out = []
+    for k in ("w1", "w2"):
+        if k in inp:
+            out.append(inp[k])
+    for k in ("w3", "w4", "w5"):
+        if k in inp:
+            out.extend(inp[k])
     return out
 
 

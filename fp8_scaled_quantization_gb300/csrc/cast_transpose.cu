@@ -181,8 +181,9 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
     if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", fn, (int)fmt);
     if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
     if (scale == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: scale is NULL", fn);
-    if (q_row == nullptr && q_col == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: q_row and q_col are both NULL", fn);
     const int64_t n = rows * cols;
+    if (n > 0 && q_row == nullptr && q_col == nullptr)
+        return fail(FP8_ERR_INVALID_ARG, "%s: q_row and q_col are both NULL", fn);
     if (n > 0 && x == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: x is NULL", fn);
     if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
     const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;

@@ -182,7 +182,8 @@ fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_forma
  *   rows, cols  >= 0.
  *   scale    device float[1].
  *   q_row    device uint8[rows, cols] or NULL (columnwise only).
- *   q_col    device uint8[cols, rows] or NULL (rowwise only); not both NULL.
+ *   q_col    device uint8[cols, rows] or NULL (rowwise only); not both NULL
+ *            unless rows * cols == 0.
  *   amax_out device float[1] or NULL: max|x|, fused.
  * Current scaling is fp8_amax(.., scale_out, scale_inv_out) followed by this
  * call.  Interior 128x128 tiles take the vector path when cols % 16 == 0,
