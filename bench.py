@@ -4,7 +4,7 @@ One step = one pass of the whole hot path over the five synthetic workloads
 (each kernel of the library runs in it):
   W1 current scaling E4M3, BF16 1024x1024               amax(+scale) -> quantize
   W2 current scaling cast+transpose E4M3, 8192x8192     amax(+scale) -> cast_transpose
-  W3 delayed scaling E4M3, 16 steps of 4096x14336       (quantize + amax + sat) -> update, x16
+  W3 delayed scaling E4M3, 16 steps of 4096x14336       quantize (+ amax, sat, history update) x16
   W4 blockwise E4M3, 128x128 on 7168x18432, 1x128 on 16384x7168
   W5 E5M2 current scaling + dequantize, 32 x 8192x8192
 value = algorithmic bytes (each kernel's reads once + writes once) / time, in
@@ -218,7 +218,8 @@ def kernel_traffic(kernel: str):
     """DRAM bytes per element from the committed ncu summary, when it was taken
     on the current source of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = {"quantize": "quantize.cu", "cast_transpose": "cast_transpose.cu", "amax": "amax_scale.cu",
+    src = {"quantize": "quantize.cu", "quantize_delayed": "quantize.cu", "cast_transpose": "cast_transpose.cu",
+           "amax": "amax_scale.cu",
            "dequantize": "dequantize.cu", "block128x128": "block_quant.cu", "block1x128": "block_quant.cu"}.get(kernel)
     if src is None or not os.path.exists(path):
         return None
@@ -334,7 +335,8 @@ def run_ours(args, rank, world):
                           "ms_per_step": round(tot_ms / args.steps, 4), "gbs": round(gbs, 1),
                           "frac": round(gbs / peak, 4)}
     traffic_per_elem = kernel_traffic(dominant)
-    per_elem_bytes = {"quantize": 3, "cast_transpose": 4, "amax": 2, "dequantize": 3}.get(dominant)
+    per_elem_bytes = {"quantize": 3, "quantize_delayed": 3, "cast_transpose": 4, "amax": 2,
+                      "dequantize": 3}.get(dominant)
     alg_per_launch = dk["bytes_per_step"] / dk["launches_per_step"]
     traffic = None
     if traffic_per_elem is not None and per_elem_bytes:
@@ -362,7 +364,9 @@ def run_ours(args, rank, world):
         "clocks": clk,
     }
     if not args.no_e2e and full_suite:
-        result["e2e"] = run_e2e(args, pipes, inp, step_bytes, world)
+        del pipes
+        torch.cuda.empty_cache()
+        result["e2e"] = run_e2e(args, inp, step_bytes, world)
     if not args.no_cpu_baseline and rank == 0 and world == 1 and full_suite:
         result["cpu_baseline"] = cpu_baseline(args, inp)
     return result
@@ -379,66 +383,58 @@ def _all_inputs(inp):
     return out
 
 
-def _outputs(pipes):
-    """The results a caller reads back: codes and scales (W5: the BF16 dequantized tensors)."""
-    p1, p2, p3, p4, p5 = (pipes[k] for k in ("W1", "W2", "W3", "W4", "W5"))
-    return {
-        "W1": [p1.q, p1.scale_inv],
-        "W2": [p2.q_row, p2.q_col, p2.scale_inv],
-        "W3": [p3.q[0], p3.amax, p3.sat, p3.scale_inv],
-        "W4": [p4.q_w, p4.si_w, p4.q_a, p4.si_a],
-        "W5": [p5.y[0], p5.scale_inv],
-    }
-
-
-def run_e2e(args, pipes, inp, step_bytes, world):
-    """The same step through the public API from pinned host memory: every step
-    copies its inputs host->device and reads its results device->host."""
+def run_e2e(args, inp, step_bytes, world):
+    """The same step through the public API with host buffers: every step
+    copies each workload's inputs host->device from pinned memory and reads
+    its results (codes and scales; W5: the dequantized BF16) back.  Copies in,
+    kernels and copies out run on three streams, one item (tensor or step)
+    at a time, ordered by events, with separate device outputs per item."""
     import torch
-    ins = {"W1": [inp["w1"]], "W2": [inp["w2"]], "W3": inp["w3"], "W4": list(inp["w4"]), "W5": inp["w5"]}
-    h_in = {k: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in v] for k, v in ins.items()}
-    for k, v in ins.items():
-        for h, d in zip(h_in[k], v):
-            h.copy_(d)
-    outs = _outputs(pipes)
-    # W3 and W5 reuse one output buffer per step / tensor, so their results are read after each one
-    h_out = {k: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in v] for k, v in outs.items()}
-    h3 = [torch.empty(pipes["W3"].q[0].shape, dtype=torch.uint8, pin_memory=True) for _ in inp["w3"]]
-    h5 = [torch.empty(pipes["W5"].y[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in inp["w5"]]
-    h2d = sum(t.numel() * t.element_size() for v in h_in.values() for t in v)
-    d2h = sum(t.numel() * t.element_size() for v in h_out.values() for t in v) + \
-        sum(t.numel() for t in h3[1:]) + sum(t.numel() * 2 for t in h5[1:])
+    from fp8_scaled_quantization_gb300 import pipelines as P, E4M3, E5M2
+    p1 = P.CurrentScaling(inp["w1"], E4M3, 0)
+    p2 = P.CurrentCastTranspose(inp["w2"], E4M3, 1)
+    p3 = P.DelayedScaling(inp["w3"], 1024, E4M3, 0, keep_codes=True)
+    p4 = P.BlockScaling(*inp["w4"], E4M3)
+    p5 = P.GradientQDQ(inp["w5"], E5M2, 0, keep_outputs=True)
+    items = [([p1.x], p1.run, [p1.q, p1.scale_inv]),
+             ([p2.x], p2.run, [p2.q_row, p2.q_col, p2.scale_inv])]
+    for k in range(len(p3.xs)):
+        last = [p3.amax, p3.sat, p3.scale_inv] if k == len(p3.xs) - 1 else []
+        items.append(([p3.xs[k]], (lambda k=k: p3.run_step(k)), [p3.q[k]] + last))
+    items.append((list(inp["w4"]), p4.run, [p4.q_w, p4.si_w, p4.q_a, p4.si_a]))
+    for k in range(len(p5.xs)):
+        last = [p5.scale_inv] if k == len(p5.xs) - 1 else []
+        items.append(([p5.xs[k]], (lambda k=k: p5.run_tensor(k)), [p5.y[k]] + last))
+    h_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins] for ins, _, _ in items]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _, _, outs in items]
+    h2d = sum(t.numel() * t.element_size() for v in h_in for t in v)
+    d2h = sum(t.numel() * t.element_size() for v in h_out for t in v)
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    prev_comp, prev_out = [None] * len(items), [None] * len(items)
 
     def e2e_step():
-        for k in ("W1", "W2", "W4"):
-            for h, d in zip(h_in[k], ins[k]):
-                d.copy_(h, non_blocking=True)
-            pipes[k].run()
-            for h, d in zip(h_out[k], outs[k]):
-                h.copy_(d, non_blocking=True)
-        p3 = pipes["W3"]
-        for h, d in zip(h_in["W3"], ins["W3"]):
-            d.copy_(h, non_blocking=True)
-        p3.hist.zero_()
-        from fp8_scaled_quantization_gb300 import fp8_quantize, fp8_update_scale_delayed
-        fp8_update_scale_delayed(p3.hist, 0, None, p3.algo, p3.fmt, p3.margin, p3.scale, p3.scale_inv)
-        for k, x in enumerate(p3.xs):
-            fp8_quantize(x, p3.fmt, p3.scale, p3.q[0], p3.amax[k:k + 1], p3.sat[k:k + 1])
-            h3[k].copy_(p3.q[0], non_blocking=True)
-            fp8_update_scale_delayed(p3.hist, k, p3.amax[k:k + 1], p3.algo, p3.fmt, p3.margin, p3.scale,
-                                     p3.scale_inv)
-        for h, d in zip(h_out["W3"][1:], outs["W3"][1:]):
-            h.copy_(d, non_blocking=True)
-        p5 = pipes["W5"]
-        from fp8_scaled_quantization_gb300 import fp8_amax, fp8_dequantize
-        for k, (h, x) in enumerate(zip(h_in["W5"], p5.xs)):
-            x.copy_(h, non_blocking=True)
-            s, si = p5.scale[k:k + 1], p5.scale_inv[k:k + 1]
-            fp8_amax(x, p5.amax[k:k + 1], p5.fmt, p5.margin, s, si)
-            fp8_quantize(x, p5.fmt, s, p5.q[0])
-            fp8_dequantize(p5.q[0], p5.fmt, si, p5.y[0])
-            h5[k].copy_(p5.y[0], non_blocking=True)
-        h_out["W5"][1].copy_(p5.scale_inv, non_blocking=True)
+        for i, (ins, fn, outs) in enumerate(items):
+            with torch.cuda.stream(s_in):
+                if prev_comp[i] is not None:
+                    s_in.wait_event(prev_comp[i])  # the last step's kernels are done with these inputs
+                for h, d in zip(h_in[i], ins):
+                    d.copy_(h, non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+            s_comp.wait_event(e_in)
+            if prev_out[i] is not None:
+                s_comp.wait_event(prev_out[i])  # the last step's results have been read back
+            fn()
+            e_c = torch.cuda.Event()
+            e_c.record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_c)
+                for h, d in zip(h_out[i], outs):
+                    h.copy_(d, non_blocking=True)
+                e_o = torch.cuda.Event()
+                e_o.record(s_out)
+            prev_comp[i], prev_out[i] = e_c, e_o
 
     steps = max(1, min(args.steps, 5))
     e2e_step()
@@ -453,7 +449,7 @@ def run_e2e(args, pipes, inp, step_bytes, world):
     return {"value": round(world * step_bytes * steps / (dt * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(dt / steps, 3),
-            "note": "pinned host buffers, one stream, copies serialised with the kernels"}
+            "note": "pinned host buffers; copies in, kernels and copies out overlapped on three streams"}
 
 
 # --------------------------------------------------------------- CPU oracle

@@ -24,7 +24,7 @@ FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 __all__ = [
     "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
     "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
-    "fp8_quantize_block", "fp8_dequantize", "launch_count", "version", "library",
+    "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "launch_count", "version", "library",
 ]
 
 
@@ -113,6 +113,20 @@ def fp8_quantize(x, fmt, scale, q_out, amax_out=None, sat_count_out=None, stream
         raise ValueError("q_out must have as many elements as x")
     _check(library().fp8_quantize(_p(x), _dt(x), x.numel(), fmt, _p(scale), _p(q_out), _p(amax_out),
                                   _p(sat_count_out), _stream(stream)))
+
+
+def fp8_quantize_delayed(x, fmt, scale, scale_inv, q_out, amax_history, step, algo=AMAX_MAX, margin=0,
+                         amax_out=None, sat_count_out=None, stream=None):
+    """One delayed-scaling step in one launch: q_out = codes of x * scale, then
+    amax(x) goes into amax_history[step % len] and scale / scale_inv are
+    overwritten with the scale of the next step."""
+    if q_out.dtype != torch.uint8 or q_out.numel() != x.numel():
+        raise ValueError("q_out must be uint8 with as many elements as x")
+    if amax_history.dtype != torch.float32:
+        raise TypeError("amax_history must be float32")
+    _check(library().fp8_quantize_delayed(_p(x), _dt(x), x.numel(), fmt, _p(scale), _p(scale_inv), _p(q_out),
+                                          _p(amax_history), amax_history.numel(), int(step), algo, margin,
+                                          _p(amax_out), _p(sat_count_out), _stream(stream)))
 
 
 def fp8_quantize_cast_transpose(x, fmt, scale, q_row, q_col, amax_out=None, stream=None):

@@ -30,6 +30,8 @@ SIGNATURES = {
     "fp8_quantize_cast_transpose": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fp8_quantize_block": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "fp8_dequantize": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp]),
+    "fp8_quantize_delayed": (c_i32, [c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32, c_i32,
+                                     c_vp, c_vp, c_vp]),
 }
 
 

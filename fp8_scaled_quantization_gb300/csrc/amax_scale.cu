@@ -21,34 +21,31 @@ namespace fp8q {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+constexpr int kLoads = 8;  // 16-byte loads in flight per thread; one chunk of 256 * 8 loads per CTA
 
-// x is 16-byte aligned here; `n` counts elements of width ESIZE from x.
+// x is 16-byte aligned here; `n` counts elements of width 2 (BF16) or 4 from x.
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 amax_kernel(const uint8_t* __restrict__ head, int head_n, const uint8_t* __restrict__ x, int64_t n,
             Workspace* ws, FinishArgs fa) {
     constexpr int kPer = BF16 ? 8 : 4;  // elements per 16-byte chunk
     const int64_t nchunks = n / kPer;
+    const int64_t cbase = (int64_t)blockIdx.x * kThreads * kLoads + threadIdx.x;
+    uint4 v[kLoads];
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+        const int64_t c = cbase + (int64_t)k * kThreads;
+        v[k] = c < nchunks ? ldg_stream(x + c * 16) : make_uint4(0, 0, 0, 0);
+    }
     uint32_t acc = 0;  // BF16: u16x2 lanes; fp32: f32 bits
-
-    const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nchunks; base += step) {
-        uint4 v[kUnroll];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const int64_t c = base + (int64_t)k * kThreads;
-            v[k] = c < nchunks ? ldg_stream(x + c * 16) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            if constexpr (BF16) {
-                acc = max_u16x2(acc, max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
-                                               max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w))));
-            } else {
-                acc = umax(acc, umax(umax(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu),
-                                     umax(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu)));
-            }
+    for (int k = 0; k < kLoads; ++k) {
+        if constexpr (BF16) {
+            acc = max_u16x2(acc, max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
+                                           max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w))));
+        } else {
+            acc = umax(acc, umax(umax(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu),
+                                 umax(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu)));
         }
     }
     uint32_t bits = BF16 ? fold_u16x2_to_f32bits(acc) : acc;
@@ -141,10 +138,9 @@ extern "C" fp8_status_t fp8_amax(const void* x, fp8_dtype_t dtype, int64_t n, fl
 
     const int per = dtype == FP8_DT_BF16 ? 8 : 4;
     const int64_t chunks = body_n / per;
-    int64_t grid = (chunks + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
-    const int64_t cap = (int64_t)sm_count() * 8;
-    if (grid > cap) grid = cap;
+    int64_t grid = (chunks + (int64_t)kThreads * kLoads - 1) / ((int64_t)kThreads * kLoads);
     if (grid < 1) grid = 1;
+    if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "fp8_amax: n too large");
 
     FinishArgs fa{amax_out, scale_out, scale_inv_out, nullptr, (int)fmt, margin};
     if (dtype == FP8_DT_BF16)

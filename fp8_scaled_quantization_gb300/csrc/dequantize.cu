@@ -17,7 +17,7 @@ namespace fp8q {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;
+constexpr int kUnits = 8;  // 16-code units per thread in the per-tensor kernel
 
 // 4 codes (one word) -> 4 products in fp32.
 template <int FMT>
@@ -64,28 +64,27 @@ __device__ __forceinline__ void dequant_one(uint8_t code, float si, uint8_t* y, 
     else reinterpret_cast<float*>(y)[e] = f[0];
 }
 
-// Per-tensor scale, q and y 16-byte aligned (any n).
+// Per-tensor scale, q and y 16-byte aligned (any n).  Each CTA owns one chunk
+// of 256 * kUnits 16-code units and issues all its loads first.
 template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 dequant_tensor_kernel(const uint8_t* __restrict__ q, int64_t n, const float* __restrict__ scale_inv,
                       uint8_t* __restrict__ y) {
-    const float si = __ldg(scale_inv);
     const int64_t nunits = n / 16;
-    const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nunits; base += step) {
-        uint4 c[kUnroll];
+    const int64_t ubase = (int64_t)blockIdx.x * kThreads * kUnits + threadIdx.x;
+    uint4 c[kUnits];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const int64_t u = base + (int64_t)k * kThreads;
-            if (u < nunits) c[k] = ldg_stream(q + u * 16);
-        }
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-            const int64_t u = base + (int64_t)k * kThreads;
-            if (u < nunits) dequant16<FMT, OUT_BF16>(c[k], si, y, u * 16);
-        }
+    for (int k = 0; k < kUnits; ++k) {
+        const int64_t u = ubase + (int64_t)k * kThreads;
+        if (u < nunits) c[k] = ldg_stream(q + u * 16);
     }
-    if (blockIdx.x == 0)
+    const float si = __ldg(scale_inv);
+#pragma unroll
+    for (int k = 0; k < kUnits; ++k) {
+        const int64_t u = ubase + (int64_t)k * kThreads;
+        if (u < nunits) dequant16<FMT, OUT_BF16>(c[k], si, y, u * 16);
+    }
+    if (blockIdx.x == gridDim.x - 1)
         for (int64_t e = nunits * 16 + threadIdx.x; e < n; e += kThreads) dequant_one<FMT, OUT_BF16>(q[e], si, y, e);
 }
 
@@ -122,8 +121,7 @@ void launch(const uint8_t* q, int64_t rows, int64_t cols, const float* si, int b
     const int64_t n = rows * cols;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (br == 0 && aligned16(q) && aligned16(y)) {
-        int64_t grid = (n / 16 + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
-        if (grid > cap) grid = cap;
+        int64_t grid = (n / 16 + (int64_t)kThreads * kUnits - 1) / ((int64_t)kThreads * kUnits);
         if (grid < 1) grid = 1;
         dequant_tensor_kernel<FMT, OUT_BF16><<<(unsigned)grid, kThreads, 0, st>>>(q, n, si, y);
         return;

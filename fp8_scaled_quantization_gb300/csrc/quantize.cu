@@ -6,8 +6,8 @@
 // counts per layer).
 //
 // HBM-bound: each thread moves 16 elements per unit (two 16-byte BF16 loads or
-// four 16-byte fp32 loads in, one 16-byte code store out), two units in
-// flight; grid-stride over a grid of 8 CTAs per SM.
+// four 16-byte fp32 loads in, one 16-byte code store out) and keeps 8 loads in
+// flight; one CTA per fixed chunk of 16384 (BF16) / 8192 (fp32) elements.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -15,76 +15,137 @@ namespace fp8q {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;  // 16-element units in flight per thread
 
-template <int FMT, bool BF16, bool AMAX, bool SAT>
+// 16-element units per thread: every thread issues all its 16-byte loads
+// (8 for BF16, 8 for fp32) before converting, and each CTA owns one fixed
+// chunk of 256 * kUnits units; the hardware scheduler balances the CTAs.
+template <bool BF16> struct VecCfg {
+    static constexpr int kUnits = BF16 ? 4 : 2;
+    static constexpr int kLoads = BF16 ? 2 : 4;  // 16-byte loads per unit
+    static constexpr int64_t kUnitsPerCta = (int64_t)kThreads * kUnits;
+};
+
+// The delayed recipe's history update, done by the last CTA of the cast
+// ("Megatron FP8" §5, update_fp8_meta): write this step's amax into slot
+// step % len, take the window maximum (NaN-propagating) or the slot, and
+// overwrite scale / scale_inv with the scale of the next step.  Every CTA has
+// read the old scale before it arrives, so the overwrite races with nothing.
+struct DelayedArgs {
+    float* hist;
+    int len;
+    int slot;
+    int algo;
+    float* scale;
+    float* scale_inv;
+};
+
+template <int FMT>
+__device__ __forceinline__ void delayed_finish(Workspace* ws, uint32_t cta_amax_bits, unsigned long long cta_sat,
+                                               const FinishArgs& fa, const DelayedArgs& da) {
+    __shared__ int s_last;
+    __shared__ float s_red[32];
+    if (threadIdx.x == 0) {
+        if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
+        if (cta_sat) atomicAdd(&ws->sat, cta_sat);
+        __threadfence();
+        s_last = atomicAdd(&ws->done, 1u) == gridDim.x * gridDim.y * gridDim.z - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) {
+        uint32_t bits = atomicExch(&ws->amax_bits, 0u);
+        const unsigned long long sat = atomicExch(&ws->sat, 0ull);
+        atomicExch(&ws->done, 0u);
+        if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
+        const float amax = __uint_as_float(bits);
+        if (fa.amax_out) *fa.amax_out = amax;
+        if (fa.sat_out) *fa.sat_out = sat;
+        da.hist[da.slot] = amax;
+    }
+    __syncthreads();  // the slot write is visible to the whole CTA
+    float eff;
+    if (da.algo == FP8_AMAX_MOST_RECENT) {
+        eff = da.hist[da.slot];
+    } else {
+        float m = -INFINITY;
+        int saw_nan = 0;
+        for (int i = threadIdx.x; i < da.len; i += blockDim.x) {
+            const float v = da.hist[i];
+            if (isnan(v)) saw_nan = 1;
+            else m = fmaxf(m, v);
+        }
+        saw_nan = __syncthreads_or(saw_nan);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (lane == 0) s_red[warp] = m;
+        __syncthreads();
+        m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        eff = saw_nan ? __uint_as_float(0x7FC00000u) : m;
+    }
+    if (threadIdx.x == 0) {
+        float sc, si;
+        scale_from_amax<FMT>(eff, fa.margin, &sc, &si);
+        *da.scale = sc;
+        *da.scale_inv = si;
+    }
+}
+
+template <int FMT, bool BF16, bool AMAX, bool SAT, bool DELAYED = false>
 __global__ void __launch_bounds__(kThreads)
 quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n,
-                    const float* __restrict__ scale_ptr, Workspace* ws, FinishArgs fa) {
-    const float scale = __ldg(scale_ptr);
+                    const float* scale_ptr, Workspace* ws, FinishArgs fa, DelayedArgs da = DelayedArgs{}) {
+    using C = VecCfg<BF16>;
     const int64_t nunits = n / 16;
+    const int64_t ubase = (int64_t)blockIdx.x * C::kUnitsPerCta + threadIdx.x;
+    uint4 v[C::kUnits][C::kLoads];
+#pragma unroll
+    for (int k = 0; k < C::kUnits; ++k) {
+        const int64_t u = ubase + (int64_t)k * kThreads;
+        if (u < nunits) {
+#pragma unroll
+            for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream(x + u * (BF16 ? 32 : 64) + h * 16);
+        }
+    }
+    const float scale = *scale_ptr;  // plain load: the delayed variant rewrites it at the end
     uint32_t am16 = 0;  // BF16: u16x2 max of |x|
     uint32_t am32 = 0;  // fp32 bits max of |x|
     uint32_t sat = 0;
-
-    const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < nunits; base += step) {
+#pragma unroll
+    for (int k = 0; k < C::kUnits; ++k) {
+        const int64_t u = ubase + (int64_t)k * kThreads;
+        if (u >= nunits) break;
         if constexpr (BF16) {
-            uint4 v[kUnroll][2];
+            Codes8 c[2];
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int64_t u = base + (int64_t)k * kThreads;
-                if (u < nunits) {
-                    v[k][0] = ldg_stream(x + u * 32);
-                    v[k][1] = ldg_stream(x + u * 32 + 16);
-                }
+            for (int h = 0; h < 2; ++h) {
+                uint32_t m;
+                c[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
+                if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale))
+                    sat += fixup_bf16x8<FMT>(v[k][h], scale, &c[h]);
+                if constexpr (AMAX) am16 = max_u16x2(am16, m);
             }
-#pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int64_t u = base + (int64_t)k * kThreads;
-                if (u >= nunits) break;
-                Codes8 c[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t m;
-                    c[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
-                    if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale))
-                        sat += fixup_bf16x8<FMT>(v[k][h], scale, &c[h]);
-                    if constexpr (AMAX) am16 = max_u16x2(am16, m);
-                }
-                stg_stream(q + u * 16, make_uint4(c[0].lo, c[0].hi, c[1].lo, c[1].hi));
-            }
+            stg_stream(q + u * 16, make_uint4(c[0].lo, c[0].hi, c[1].lo, c[1].hi));
         } else {
-            uint4 v[kUnroll][4];
+            uint32_t w[4];
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int64_t u = base + (int64_t)k * kThreads;
-                if (u < nunits) {
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) v[k][h] = ldg_stream(x + u * 64 + h * 16);
-                }
+            for (int h = 0; h < 4; ++h) {
+                float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
+                                       __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
+                uint32_t m;
+                w[h] = cvt_f32x4<FMT>(f, scale, &m);
+                if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w[h]);
+                if constexpr (AMAX) am32 = umax(am32, m);
             }
-#pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int64_t u = base + (int64_t)k * kThreads;
-                if (u >= nunits) break;
-                uint32_t w[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
-                                           __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
-                    uint32_t m;
-                    w[h] = cvt_f32x4<FMT>(f, scale, &m);
-                    if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w[h]);
-                    if constexpr (AMAX) am32 = umax(am32, m);
-                }
-                stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
-            }
+            stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
         }
     }
 
-    // Tail (< 16 elements): block 0.
-    if (blockIdx.x == 0) {
+    // Tail (< 16 elements): the last CTA.
+    if (blockIdx.x == gridDim.x - 1) {
         for (int64_t i = nunits * 16 + threadIdx.x; i < n; i += kThreads) {
             float xv;
             uint32_t b;
@@ -103,22 +164,24 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
         }
     }
 
-    if constexpr (AMAX || SAT) {
+    if constexpr (AMAX || SAT || DELAYED) {
         __shared__ uint32_t red[32];
         __shared__ unsigned long long red64[32];
         uint32_t bits = umax(am32, BF16 ? fold_u16x2_to_f32bits(am16) : 0u);
         bits = block_max_u32(bits, red);
         unsigned long long total = SAT ? block_sum_u64((unsigned long long)sat, red64) : 0ull;
-        grid_finish(ws, bits, total, fa);
+        if constexpr (DELAYED) delayed_finish<FMT>(ws, bits, total, fa, da);
+        else grid_finish(ws, bits, total, fa);
     }
 }
 
 // Element-at-a-time path for pointers that are not 16-byte aligned.
-template <int FMT, bool BF16>
+template <int FMT, bool BF16, bool DELAYED = false>
 __global__ void __launch_bounds__(kThreads)
 quantize_scalar_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n,
-                       const float* __restrict__ scale_ptr, Workspace* ws, FinishArgs fa, int reduce) {
-    const float scale = __ldg(scale_ptr);
+                       const float* scale_ptr, Workspace* ws, FinishArgs fa, int reduce,
+                       DelayedArgs da = DelayedArgs{}) {
+    const float scale = *scale_ptr;
     uint32_t am = 0, sat = 0;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
         float xv;
@@ -136,12 +199,13 @@ quantize_scalar_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, i
         sat += s;
         am = umax(am, b);
     }
-    if (reduce) {
+    if (reduce || DELAYED) {
         __shared__ uint32_t red[32];
         __shared__ unsigned long long red64[32];
         uint32_t bits = block_max_u32(am, red);
         unsigned long long total = block_sum_u64((unsigned long long)sat, red64);
-        grid_finish(ws, bits, total, fa);
+        if constexpr (DELAYED) delayed_finish<FMT>(ws, bits, total, fa, da);
+        else grid_finish(ws, bits, total, fa);
     }
 }
 
@@ -186,10 +250,10 @@ extern "C" fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n
 
     if (aligned16(x) && aligned16(q_out)) {
         const int64_t units = n / 16;
-        int64_t grid = (units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
-        const int64_t cap = (int64_t)sm_count() * 8;
-        if (grid > cap) grid = cap;
+        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
+        int64_t grid = (units + per_cta - 1) / per_cta;
         if (grid < 1) grid = 1;
+        if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "fp8_quantize: n too large");
         const bool am = amax_out != nullptr, sc = sat_count_out != nullptr;
         if (fmt == FP8_E4M3) {
             if (bf16) launch_vec<kE4M3, true>(am, sc, (unsigned)grid, st, xp, q_out, n, scale, ws, fa);
@@ -213,4 +277,66 @@ extern "C" fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n
         }
     }
     return after_launch("fp8_quantize");
+}
+
+extern "C" fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
+                                             float* scale, float* scale_inv, uint8_t* q_out, float* amax_history,
+                                             int history_len, int64_t step, fp8_amax_algo_t algo, int margin,
+                                             float* amax_out, unsigned long long* sat_count_out, void* stream) {
+    const char* fn = "fp8_quantize_delayed";
+    if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", fn, (int)fmt);
+    if (n < 0) return fail(FP8_ERR_INVALID_ARG, "%s: n < 0", fn);
+    if (scale == nullptr || scale_inv == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: scale / scale_inv is NULL", fn);
+    if (n > 0 && (x == nullptr || q_out == nullptr)) return fail(FP8_ERR_INVALID_ARG, "%s: x / q_out is NULL", fn);
+    if (amax_history == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: amax_history is NULL", fn);
+    if (history_len < 1 || history_len > 65536) return fail(FP8_ERR_INVALID_ARG, "%s: history_len must be in [1, 65536]", fn);
+    if (step < 0) return fail(FP8_ERR_INVALID_ARG, "%s: step < 0", fn);
+    if (algo != FP8_AMAX_MAX && algo != FP8_AMAX_MOST_RECENT) return fail(FP8_ERR_INVALID_ARG, "%s: unknown algo %d", fn, (int)algo);
+    if (!valid_margin(margin)) return fail(FP8_ERR_INVALID_ARG, "%s: margin out of [-126, 126]", fn);
+    const int es = dtype_size(dtype);
+    if (reinterpret_cast<uintptr_t>(x) % es) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    fp8_status_t s;
+    Workspace* ws = stream_workspace(st, &s);
+    if (!ws) return s;
+    FinishArgs fa{amax_out, nullptr, nullptr, sat_count_out, (int)fmt, margin};
+    DelayedArgs da{amax_history, history_len, (int)(step % history_len), (int)algo, scale, scale_inv};
+    const uint8_t* xp = static_cast<const uint8_t*>(x);
+    const bool bf16 = dtype == FP8_DT_BF16, sc = sat_count_out != nullptr;
+    if (aligned16(x) && aligned16(q_out)) {
+        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
+        int64_t grid = (n / 16 + per_cta - 1) / per_cta;
+        if (grid < 1) grid = 1;
+        if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "%s: n too large", fn);
+        const unsigned g = (unsigned)grid;
+#define FP8Q_LAUNCH_DELAYED(F, B)                                                                                  \
+    do {                                                                                                           \
+        if (sc) quantize_vec_kernel<F, B, true, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, da); \
+        else quantize_vec_kernel<F, B, true, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, da);  \
+    } while (0)
+        if (fmt == FP8_E4M3) {
+            if (bf16) FP8Q_LAUNCH_DELAYED(kE4M3, true);
+            else FP8Q_LAUNCH_DELAYED(kE4M3, false);
+        } else {
+            if (bf16) FP8Q_LAUNCH_DELAYED(kE5M2, true);
+            else FP8Q_LAUNCH_DELAYED(kE5M2, false);
+        }
+#undef FP8Q_LAUNCH_DELAYED
+    } else {
+        int64_t grid = (n + kThreads - 1) / kThreads;
+        const int64_t cap = (int64_t)sm_count() * 8;
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        const unsigned g = (unsigned)grid;
+        if (fmt == FP8_E4M3) {
+            if (bf16) quantize_scalar_kernel<kE4M3, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
+            else quantize_scalar_kernel<kE4M3, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
+        } else {
+            if (bf16) quantize_scalar_kernel<kE5M2, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
+            else quantize_scalar_kernel<kE5M2, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
+        }
+    }
+    return after_launch(fn);
 }

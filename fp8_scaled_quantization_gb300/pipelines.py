@@ -20,7 +20,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import (AMAX_MAX, E4M3, E5M2, fp8_amax, fp8_dequantize, fp8_quantize, fp8_quantize_block,
-               fp8_quantize_cast_transpose, fp8_update_scale_delayed)
+               fp8_quantize_cast_transpose, fp8_quantize_delayed, fp8_update_scale_delayed)
 
 
 def _f32(dev, n=1, fill=None):
@@ -100,11 +100,14 @@ class DelayedScaling:
 
     A run starts from a zero history (scale 1 at step 0) and, per step k,
     casts x_k with the current scale while recording amax_k and the saturated
-    count, then writes amax_k into slot k % len and derives the next scale."""
+    count, then writes amax_k into slot k % len and derives the next scale.
+    With fused=True (the default) each step is one fp8_quantize_delayed
+    launch; fused=False issues fp8_quantize + fp8_update_scale_delayed."""
 
     def __init__(self, xs: list, history_len: int = 1024, fmt: int = E4M3, margin: int = 0,
-                 algo: int = AMAX_MAX, keep_codes: bool = False, record_scales: bool = False):
-        self.xs, self.fmt, self.margin, self.algo = xs, fmt, margin, algo
+                 algo: int = AMAX_MAX, keep_codes: bool = False, record_scales: bool = False,
+                 fused: bool = True):
+        self.xs, self.fmt, self.margin, self.algo, self.fused = xs, fmt, margin, algo, fused
         dev = xs[0].device
         self.hist = torch.zeros(history_len, dtype=torch.float32, device=dev)
         self.scale, self.scale_inv = _f32(dev), _f32(dev)
@@ -116,24 +119,37 @@ class DelayedScaling:
         self.q = [torch.empty(xs[0].shape, dtype=torch.uint8, device=dev) for _ in range(n)]
 
     def run(self, timer=None):
-        self.hist.zero_()
-        _t(timer, "update_delayed", lambda: fp8_update_scale_delayed(self.hist, 0, None, self.algo, self.fmt,
-                                                                     self.margin, self.scale, self.scale_inv))
-        for k, x in enumerate(self.xs):
-            q = self.q[k % len(self.q)]
-            if self.scales is not None:
-                self.scales[k:k + 1].copy_(self.scale)
-            _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, self.scale, q, self.amax[k:k + 1],
-                                                       self.sat[k:k + 1]))
-            _t(timer, "update_delayed", lambda: fp8_update_scale_delayed(
-                self.hist, k, self.amax[k:k + 1], self.algo, self.fmt, self.margin, self.scale, self.scale_inv))
+        for k in range(len(self.xs)):
+            self.run_step(k, timer)
+
+    def run_step(self, k: int, timer=None):
+        """Step k of the sequence (step 0 also resets the history and the scale)."""
+        if k == 0:
+            self.hist.zero_()
+            _t(timer, "update_delayed", lambda: fp8_update_scale_delayed(self.hist, 0, None, self.algo, self.fmt,
+                                                                         self.margin, self.scale, self.scale_inv))
+        x, q = self.xs[k], self.q[k % len(self.q)]
+        if self.scales is not None:
+            self.scales[k:k + 1].copy_(self.scale)
+        if self.fused:
+            _t(timer, "quantize_delayed", lambda: fp8_quantize_delayed(
+                x, self.fmt, self.scale, self.scale_inv, q, self.hist, k, self.algo, self.margin,
+                self.amax[k:k + 1], self.sat[k:k + 1]))
+            return
+        _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, self.scale, q, self.amax[k:k + 1],
+                                                   self.sat[k:k + 1]))
+        _t(timer, "update_delayed", lambda: fp8_update_scale_delayed(
+            self.hist, k, self.amax[k:k + 1], self.algo, self.fmt, self.margin, self.scale, self.scale_inv))
 
     def bytes(self) -> KernelBytes:
         b = KernelBytes()
+        hist_bytes = self.hist.numel() * 4 + 4 + 8
         for x in self.xs:
-            b.add("quantize", x.numel() * (esize(x) + 1))
-        hist_bytes = self.hist.numel() * 4
-        b.add("update_delayed", hist_bytes + 4 + 8, len(self.xs) + 1)
+            if self.fused:
+                b.add("quantize_delayed", x.numel() * (esize(x) + 1) + hist_bytes)
+            else:
+                b.add("quantize", x.numel() * (esize(x) + 1))
+        b.add("update_delayed", hist_bytes, 1 if self.fused else len(self.xs) + 1)
         return b
 
 
@@ -174,12 +190,15 @@ class GradientQDQ:
         self.scale_inv = torch.empty(len(xs), dtype=torch.float32, device=dev)
 
     def run(self, timer=None):
-        for k, x in enumerate(self.xs):
-            q, y = self.q[k % len(self.q)], self.y[k % len(self.y)]
-            s, si = self.scale[k:k + 1], self.scale_inv[k:k + 1]
-            _t(timer, "amax", lambda: fp8_amax(x, self.amax[k:k + 1], self.fmt, self.margin, s, si))
-            _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
-            _t(timer, "dequantize", lambda: fp8_dequantize(q, self.fmt, si, y))
+        for k in range(len(self.xs)):
+            self.run_tensor(k, timer)
+
+    def run_tensor(self, k: int, timer=None):
+        x, q, y = self.xs[k], self.q[k % len(self.q)], self.y[k % len(self.y)]
+        s, si = self.scale[k:k + 1], self.scale_inv[k:k + 1]
+        _t(timer, "amax", lambda: fp8_amax(x, self.amax[k:k + 1], self.fmt, self.margin, s, si))
+        _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
+        _t(timer, "dequantize", lambda: fp8_dequantize(q, self.fmt, si, y))
 
     def bytes(self) -> KernelBytes:
         b = KernelBytes()

@@ -170,6 +170,32 @@ fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_forma
                           unsigned long long* sat_count_out, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Delayed scaling, fused: the cast of one step and the history update      */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §5: per step, cast with the scale derived from the amax
+ * history, record this step's amax into slot step % history_len, and derive
+ * the scale of the next step -- here in one launch: the last CTA of the cast
+ * performs the update of fp8_update_scale_delayed.
+ *
+ * Equivalent, bit for bit, to
+ *   fp8_quantize(x, .., scale, q_out, tmp_amax, sat_count_out)
+ *   fp8_update_scale_delayed(amax_history, history_len, step, tmp_amax, algo,
+ *                            fmt, margin, scale, scale_inv)
+ *
+ *   scale, scale_inv  device float[1] each, read and written: on entry the
+ *                     scale of this step (scale_inv is not read), on return
+ *                     the scale / scale_inv of the next step.
+ *   amax_history      device float[history_len], updated in place.
+ *   amax_out          device float[1] or NULL: this step's amax.
+ *   sat_count_out     device uint64[1] or NULL: as in fp8_quantize.
+ *   Other arguments as in fp8_quantize / fp8_update_scale_delayed.
+ * One kernel launch. */
+fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
+                                  float* scale, float* scale_inv, uint8_t* q_out, float* amax_history,
+                                  int history_len, int64_t step, fp8_amax_algo_t algo, int margin,
+                                  float* amax_out, unsigned long long* sat_count_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Quantize with rowwise + columnwise (transposed) outputs                  */
 /* ------------------------------------------------------------------------ */
 /* "Megatron FP8" §6 (the weight-gradient GEMM consumes transpose(dy_fp8)) and

@@ -315,6 +315,52 @@ def test_delayed_sequence_matches_oracle(cuda, oracle, algo, hist_len):
         assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("algo", [fq.AMAX_MAX, fq.AMAX_MOST_RECENT])
+@pytest.mark.parametrize("hist_len,shape", [(1, (96, 160)), (4, (33, 77)), (1024, (96, 160))])
+def test_fused_delayed_sequence_matches_oracle(cuda, oracle, dtype, algo, hist_len, shape):
+    steps, margin, fmt = 10, 1, E5M2
+    hist = torch.zeros(hist_len, dtype=torch.float32, device=cuda)
+    s, si = torch.empty(1, device=cuda), torch.empty(1, device=cuda)
+    am = torch.empty(1, device=cuda)
+    sat = torch.empty(1, dtype=torch.int64, device=cuda)
+    h_ref = np.zeros(hist_len, dtype=np.float32)
+    fq.fp8_update_scale_delayed(hist, 0, None, algo, fmt, margin, s, si)
+    ws, wsi = oracle.update_delayed(h_ref, 0, None, algo, fmt, margin)
+    g = torch.Generator(device="cpu").manual_seed(hist_len)
+    for k in range(steps):
+        x = (torch.randn(shape, generator=g) * 1e-3 * 1.5 ** k).to(dtype).to(cuda)
+        if k == 6:
+            x.view(-1)[5] = float("inf")
+        q = torch.empty(shape, dtype=torch.uint8, device=cuda)
+        fq.fp8_quantize_delayed(x, fmt, s, si, q, hist, k, algo, margin, am, sat)
+        torch.cuda.synchronize()
+        xb = host_bits(x)
+        wq, wsat = oracle.quantize(xb, fmt, ws)
+        assert np.array_equal(q.cpu().numpy(), wq), k
+        assert sat.item() == wsat
+        a = oracle.amax(xb)
+        assert f32_bits(am.item()) == f32_bits(a)
+        ws, wsi = oracle.update_delayed(h_ref, k, a, algo, fmt, margin)
+        assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi)), k
+        assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32))
+
+
+def test_fused_delayed_unaligned(cuda, oracle):
+    base = random_input(10_001, torch.bfloat16, 5, cuda)
+    x = base[1:]
+    hist = torch.zeros(8, device=cuda)
+    s, si = dev_scalar(0.25, cuda), torch.empty(1, device=cuda)
+    q = torch.empty(x.numel(), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_delayed(x, E4M3, s, si, q, hist, 3, fq.AMAX_MAX, 0)
+    torch.cuda.synchronize()
+    xb = host_bits(x)
+    assert np.array_equal(q.cpu().numpy(), oracle.quantize(xb, E4M3, np.float32(0.25))[0])
+    h = np.zeros(8, np.float32)
+    ws, wsi = oracle.update_delayed(h, 3, oracle.amax(xb), oracle.ALGO_MAX, E4M3, 0)
+    assert (s.item(), si.item()) == (float(ws), float(wsi))
+
+
 def test_current_equals_delayed_history_one(cuda):
     x = random_input(33_333, torch.bfloat16, 4, cuda)
     am, s1, si1, s2, si2 = (torch.empty(1, device=cuda) for _ in range(5))

@@ -56,6 +56,12 @@ BAD = 0x1000  # never dereferenced: every call below is rejected on the host fir
     (lambda L: L.fp8_update_scale_delayed(BAD, 4, -1, None, 0, 0, 0, BAD, BAD, None), 1, "step < 0"),
     (lambda L: L.fp8_update_scale_delayed(BAD, 4, 0, None, 3, 0, 0, BAD, BAD, None), 1, "unknown algo"),
     (lambda L: L.fp8_update_scale_delayed(BAD, 4, 0, None, 0, 0, 0, None, BAD, None), 1, "NULL"),
+    (lambda L: L.fp8_quantize_delayed(BAD, 0, 10, 0, BAD, BAD, BAD, BAD, 0, 0, 0, 0, None, None, None), 1,
+     "history_len"),
+    (lambda L: L.fp8_quantize_delayed(BAD, 0, 10, 0, None, BAD, BAD, BAD, 4, 0, 0, 0, None, None, None), 1,
+     "scale / scale_inv is NULL"),
+    (lambda L: L.fp8_quantize_delayed(BAD, 0, 10, 0, BAD, BAD, BAD, BAD, 4, 0, 2, 0, None, None, None), 1,
+     "unknown algo"),
     (lambda L: L.fp8_quantize_cast_transpose(BAD, 0, 4, 4, 0, BAD, None, None, None, None), 1, "both NULL"),
     (lambda L: L.fp8_quantize_cast_transpose(BAD, 0, -4, 4, 0, BAD, BAD, None, None, None), 1, "negative"),
     (lambda L: L.fp8_quantize_block(BAD, 0, 4, 4, 64, 64, 0, BAD, BAD, None), 2, "block shape"),
@@ -112,13 +118,13 @@ def test_pipeline_byte_accounting_full_size():
     N1, N2, N3, N5 = 1024 * 1024, 8192 * 8192, 4096 * 14336, 8192 * 8192
     assert b["W1"].total == 5 * N1
     assert b["W2"].total == 6 * N2
-    assert b["W3"].per_kernel["quantize"] == (16 * 3 * N3, 16)
+    assert b["W3"].per_kernel["quantize_delayed"] == (16 * (3 * N3 + 4 * 1024 + 12), 16)
     assert b["W4"].per_kernel["block128x128"][0] == 3 * 7168 * 18432 + 4 * 56 * 144
     assert b["W4"].per_kernel["block1x128"][0] == 3 * 16384 * 7168 + 4 * 16384 * 56
     assert b["W5"].total == 32 * 8 * N5
     total = sum(x.total for x in b.values())
     assert 21.0e9 < total < 21.3e9
-    assert sum(x.launches for x in b.values()) == 2 + 2 + (16 + 17) + 2 + 96
+    assert sum(x.launches for x in b.values()) == 2 + 2 + (16 + 1) + 2 + 96
 
 
 # ------------------------------------------------------------- multi-rank
