@@ -24,7 +24,7 @@ FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 __all__ = [
     "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
     "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
-    "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "launch_count", "version", "library",
+    "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_amax_noalloc", "launch_count", "version", "library",
 ]
 
 
@@ -93,6 +93,15 @@ def fp8_amax(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None
     """amax_out[0] = max|x|; with scale_out / scale_inv_out, also the current scale."""
     _check(library().fp8_amax(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
                               _p(scale_out), _p(scale_inv_out), _stream(stream)))
+
+
+def fp8_amax_noalloc(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):
+    """fp8_amax for callers that cannot allocate device memory: the library
+    uses a fixed file-scope scratch array instead of a per-stream workspace.
+    At most 2**28 elements; make the first call on a device before any stream
+    capture; calls that overlap on the GPU race on the shared scratch."""
+    _check(library().fp8_amax_noalloc(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
+                                      _p(scale_out), _p(scale_inv_out), _stream(stream)))
 
 
 def fp8_update_scale_delayed(amax_history, step, new_amax, algo, fmt, margin, scale_out, scale_inv_out,

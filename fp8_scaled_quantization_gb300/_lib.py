@@ -32,6 +32,7 @@ SIGNATURES = {
     "fp8_dequantize": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp]),
     "fp8_quantize_delayed": (c_i32, [c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_i64, c_i32, c_i32,
                                      c_vp, c_vp, c_vp]),
+    "fp8_amax_noalloc": (c_i32, [c_vp, c_i32, c_i64, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
 }
 
 

@@ -264,6 +264,36 @@ fp8_status_t fp8_dequantize(const uint8_t* q, fp8_format_t fmt, int64_t rows, in
                             const float* scale_inv, int block_rows, int block_cols, void* y,
                             fp8_dtype_t out_dtype, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* amax without any device allocation                                       */
+/* ------------------------------------------------------------------------ */
+/* The pages have no counterpart to this entry point; it serves callers that
+ * cannot let a library allocate device memory -- code running while a stream
+ * is captured in the global capture mode (where cudaMalloc is an illegal
+ * call), engines and plugins that work inside a fixed, pre-planned memory
+ * budget, and frameworks whose allocator must own every device buffer.
+ *
+ * Same arguments, results and numerics as fp8_amax (bit-identical outputs).
+ * Differences:
+ *   - It allocates nothing (no cudaMalloc / cudaFree, no library allocator).
+ *     Its scratch is a fixed 16.25 KB file-scope device array (one arrival
+ *     counter and 4096 per-CTA partial maxima) that every GPU which loads
+ *     the library holds until the process exits.
+ *   - n must not exceed 2^28 (268,435,456) elements: each CTA reduces a fixed
+ *     slice of 65,536 elements and the scratch has room for 4096 CTAs.
+ *     Larger n returns FP8_ERR_UNSUPPORTED without touching the device.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, which may load the library's GPU code); make that
+ *     first call before any stream capture on that device.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents.  Each call clears the counter on its stream before its kernel.
+ *     Calls that overlap on the GPU (different streams, or graphs replayed
+ *     concurrently) race on the scratch and give wrong results; serialise them.
+ * One memset node plus one kernel launch. */
+fp8_status_t fp8_amax_noalloc(const void* x, fp8_dtype_t dtype, int64_t n, float* amax_out,
+                              fp8_format_t fmt, int margin, float* scale_out, float* scale_inv_out,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif
