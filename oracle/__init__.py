@@ -75,6 +75,13 @@ def lib():
         L.oref_quantize_block.restype = None
         L.oref_dequantize.argtypes = [vp, i32, i64, i64, vp, i32, i32, vp, i32]
         L.oref_dequantize.restype = None
+        L.oref_e8m0_decode.argtypes, L.oref_e8m0_decode.restype = [u8], f64
+        L.oref_quantize_mx.argtypes = [vp, i32, i64, i64, i32, vp, vp]
+        L.oref_quantize_mx.restype = None
+        L.oref_dequantize_mx.argtypes = [vp, vp, i64, i64, i32, vp, i32]
+        L.oref_dequantize_mx.restype = None
+        L.oref_block128_scales_to_mx.argtypes = [vp, i64, i64, vp]
+        L.oref_block128_scales_to_mx.restype = i64
         _lib = L
     return _lib
 
@@ -305,3 +312,54 @@ def dequantize(q: np.ndarray, fmt: int, scale_inv, br: int = 0, bc: int = 0, out
         with ThreadPoolExecutor(len(parts)) as ex:
             list(ex.map(run, parts))
     return y.reshape(q.shape)
+
+
+# --------------------------------------------------------------------------- MXFP8
+
+MX_BLOCK = 32
+
+
+def e8m0_decode(code: int) -> float:
+    return lib().oref_e8m0_decode(code)
+
+
+def quantize_mx(x: np.ndarray, fmt: int, threads: int = 1):
+    """Rowwise MX quantize of [rows, cols]: (codes [rows, cols], E8M0 scales [rows, ceil(cols/32)])."""
+    assert x.ndim == 2
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    dt = _dtype_of(x)
+    nb = -(-cols // MX_BLOCK)
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty((rows, nb), dtype=np.uint8)
+    L = lib()
+
+    def run(se):
+        s, e = se
+        L.oref_quantize_mx(_ptr(x) + s * cols * x.itemsize, dt, e - s, cols, fmt, _ptr(q) + s * cols,
+                           _ptr(sc) + s * nb)
+
+    parts = _chunks(rows, threads)
+    if len(parts) == 1:
+        run(parts[0])
+    else:
+        with ThreadPoolExecutor(len(parts)) as ex:
+            list(ex.map(run, parts))
+    return q, sc
+
+
+def dequantize_mx(q: np.ndarray, scales: np.ndarray, fmt: int, out_dt: int = BF16) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, cols = q.shape
+    y = np.empty((rows, cols), dtype=np.uint16 if out_dt == BF16 else np.float32)
+    lib().oref_dequantize_mx(_ptr(q), _ptr(sc), rows, cols, fmt, _ptr(y), out_dt)
+    return y
+
+
+def block128_scales_to_mx(scale_inv: np.ndarray, rows: int, cols: int):
+    """E8M0 [rows, ceil(cols/32)] scales from 128x128 fp32 scale_inv; returns (scales, non-power-of-two blocks)."""
+    si = np.ascontiguousarray(scale_inv, dtype=np.float32)
+    out = np.empty((rows, -(-cols // MX_BLOCK)), dtype=np.uint8)
+    bad = lib().oref_block128_scales_to_mx(_ptr(si), rows, cols, _ptr(out))
+    return out, int(bad)

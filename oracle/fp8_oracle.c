@@ -436,3 +436,128 @@ void oref_dequantize(const uint8_t* q, int fmt, int64_t rows, int64_t cols, cons
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8: one E8M0 power-of-two scale per 32 consecutive elements           */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §10 and §16: every 32 consecutive elements share one E8M0
+ * scale -- 8 exponent bits, no mantissa, no sign, 2^-127 .. 2^127 -- the OCP
+ * Microscaling (MX) format; applying it is an exponent add.  "Low Precision
+ * Training and Rollout", "MXFP8 (Blackwell only)": E4M3 values with UE8M0
+ * scales per 32-element group.
+ *
+ * Readings (the pages give the format, not the rule that picks the scale):
+ *   - the OCP MX rule: shared_exp = floor(log2(amax_block)) - emax_elem,
+ *     emax_elem = unbiased exponent of the element format's largest finite
+ *     value (8 for E4M3, 15 for E5M2), clamped to [-127, 127]; an all-zero
+ *     block takes -127;
+ *   - elements: encode_saturating(fl32(x * 2^-shared_exp));
+ *   - a block holding a NaN or an infinity gets the NaN scale code 0xFF and
+ *     every element of that block the NaN code 0x7F;
+ *   - E8M0 code = shared_exp + 127; code 0xFF is NaN. */
+
+#define OREF_MX_BLOCK 32
+
+/* E8M0 value: 2^(code - 127); code 255 is NaN. */
+double oref_e8m0_decode(uint8_t code) {
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* The shared exponent of a block from its amax (finite, >= 0). */
+static int mx_shared_exp(double amax, const fmt_info* f) {
+    if (amax == 0.0) return -127;
+    int ex;
+    frexp(amax, &ex); /* amax in [2^(ex-1), 2^ex) => floor(log2(amax)) = ex - 1 */
+    int mex;
+    frexp(f->max_finite, &mex);
+    int e_max_elem = mex - 1; /* 8 for E4M3 (448 = 1.75 * 2^8), 15 for E5M2 */
+    int se = (ex - 1) - e_max_elem;
+    if (se < -127) se = -127;
+    if (se > 127) se = 127;
+    return se;
+}
+
+/* Rowwise MX quantize of a row-major [rows, cols] input: blocks are 32
+ * consecutive elements of a row (the last block of a row may be shorter);
+ * scales are row-major [rows, ceil(cols / 32)] E8M0 codes. */
+void oref_quantize_mx(const void* x, int dt, int64_t rows, int64_t cols, int fmt, uint8_t* q, uint8_t* scales) {
+    fmt_info f = make_info(fmt);
+    int64_t nb = (cols + OREF_MX_BLOCK - 1) / OREF_MX_BLOCK;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            int64_t c0 = b * OREF_MX_BLOCK, c1 = c0 + OREF_MX_BLOCK < cols ? c0 + OREF_MX_BLOCK : cols;
+            double amax = 0.0;
+            int special = 0;
+            for (int64_t c = c0; c < c1; ++c) {
+                double v = fabs((double)load_elem(x, dt, r * cols + c));
+                if (isnan(v) || isinf(v)) special = 1;
+                else if (v > amax) amax = v;
+            }
+            if (special) {
+                scales[r * nb + b] = 0xFF;
+                for (int64_t c = c0; c < c1; ++c) q[r * cols + c] = OREF_NAN_CODE;
+                continue;
+            }
+            int se = mx_shared_exp(amax, &f);
+            scales[r * nb + b] = (uint8_t)(se + 127);
+            float m = (float)ldexp(1.0, -se); /* 2^-se, exact in fp32 for |se| <= 127 */
+            for (int64_t c = c0; c < c1; ++c) {
+                float p = load_elem(x, dt, r * cols + c) * m; /* one fp32 multiply */
+                q[r * cols + c] = encode_saturating(p, &f);
+            }
+        }
+    }
+}
+
+/* MX dequantize (rowwise layout): y = decode(q) * 2^(scale - 127), one fp32
+ * multiply, then BF16 (round to nearest even) or fp32.  A NaN scale makes
+ * the block NaN; NaN results use the canonical NaN of the output type. */
+void oref_dequantize_mx(const uint8_t* q, const uint8_t* scales, int64_t rows, int64_t cols, int fmt, void* y,
+                        int out_dt) {
+    int64_t nb = (cols + OREF_MX_BLOCK - 1) / OREF_MX_BLOCK;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            float s = (float)oref_e8m0_decode(scales[r * nb + c / OREF_MX_BLOCK]);
+            float v = oref_decode(q[r * cols + c], fmt) * s;
+            if (out_dt == OREF_BF16) {
+                ((uint16_t*)y)[r * cols + c] = oref_f32_to_bf16(v);
+            } else if (isnan(v)) {
+                uint32_t u = 0x7FFFFFFFu;
+                memcpy(&((float*)y)[r * cols + c], &u, sizeof u);
+            } else {
+                ((float*)y)[r * cols + c] = v;
+            }
+        }
+    }
+}
+
+/* Lossless re-blocking of 128 x 128 block scales into 1 x 32 E8M0 scales
+ * ("Low Precision Training and Rollout", "MXFP8 (Blackwell only)": block-FP8
+ * [128,128] sources are rescaled to [1,32] without dequantizing when the
+ * scales are powers of two).  The codes are unchanged; each 1 x 32 block takes
+ * the E8M0 code of its 128 x 128 block's scale_inv.  A scale_inv that is not
+ * a power of two in [2^-127, 2^127] cannot be represented: its blocks get
+ * 0xFF and the function returns how many 128 x 128 blocks were like that. */
+int64_t oref_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t cols, uint8_t* mx_scales) {
+    int64_t nbc128 = (cols + 127) / 128, nb32 = (cols + OREF_MX_BLOCK - 1) / OREF_MX_BLOCK;
+    int64_t bad = 0;
+    int64_t nbr128 = (rows + 127) / 128;
+    for (int64_t i = 0; i < nbr128; ++i)
+        for (int64_t j = 0; j < nbc128; ++j) {
+            double s = (double)scale_inv[i * nbc128 + j];
+            int ex;
+            double frac = frexp(s, &ex); /* s = frac * 2^ex, frac in [0.5, 1) */
+            if (!(s > 0.0) || isinf(s) || frac != 0.5 || ex - 1 < -127 || ex - 1 > 127) ++bad;
+        }
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb32; ++b) {
+            double s = (double)scale_inv[(r / 128) * nbc128 + (b * OREF_MX_BLOCK) / 128];
+            int ex;
+            double frac = frexp(s, &ex);
+            uint8_t code = 0xFF;
+            if (s > 0.0 && !isinf(s) && frac == 0.5 && ex - 1 >= -127 && ex - 1 <= 127) code = (uint8_t)(ex - 1 + 127);
+            mx_scales[r * nb32 + b] = code;
+        }
+    return bad;
+}
