@@ -288,9 +288,14 @@ def run_ours(args, rank, world):
         step()
     torch.cuda.synchronize()
 
+    # Per-launch events sit between kernels and add small gaps, so the headline
+    # region carries only its two bracketing events; per-kernel and per-workload
+    # durations come from a second pass of the same steps with events around
+    # every launch, right after it.
+    ksteps = max(3, min(args.steps, 20))
     timer, vtimer = EventTimer(), EventTimer()
-    timer.reserve(2 * kb.launches * args.steps + 8)
-    vtimer.reserve(2 * len(pipes) * args.steps + 8)
+    timer.reserve(2 * kb.launches * ksteps + 8)
+    vtimer.reserve(2 * len(pipes) * ksteps + 8)
     gpu_uuid = None
     try:
         gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -307,7 +312,7 @@ def run_ours(args, rank, world):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(args.steps):
-        step(timer, vtimer)
+        step()
     t1.record()
     torch.cuda.synchronize()
     launches = fq.launch_count() - launches0
@@ -316,13 +321,16 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
     ms_max = max_over_ranks(ms, world)
+    for _ in range(ksteps):
+        step(timer, vtimer)
+    torch.cuda.synchronize()
 
     peak, peak_kind = measured_hbm_peak()
     kernels = {}
     for name, (tot_ms, n) in timer.totals().items():
         nbytes, nl = kb.per_kernel[name]
-        gbs = nbytes * args.steps / (tot_ms * 1e-3) / 1e9
-        kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": round(tot_ms / args.steps, 4),
+        gbs = nbytes * ksteps / (tot_ms * 1e-3) / 1e9
+        kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": round(tot_ms / ksteps, 4),
                          "avg_launch_us": round(tot_ms * 1e3 / n, 2), "gbs": round(gbs, 1),
                          "frac": round(gbs / peak, 4)}
     dominant = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
@@ -330,9 +338,9 @@ def run_ours(args, rank, world):
     variants = {}
     for name, (tot_ms, n) in vtimer.totals().items():
         cb = compulsory_bytes({name: pipes[name]})
-        gbs = cb * args.steps / (tot_ms * 1e-3) / 1e9
+        gbs = cb * ksteps / (tot_ms * 1e-3) / 1e9
         variants[name] = {"compulsory_bytes": cb, "kernel_bytes": per_variant_bytes[name].total,
-                          "ms_per_step": round(tot_ms / args.steps, 4), "gbs": round(gbs, 1),
+                          "ms_per_step": round(tot_ms / ksteps, 4), "gbs": round(gbs, 1),
                           "frac": round(gbs / peak, 4)}
     traffic_per_elem = kernel_traffic(dominant)
     per_elem_bytes = {"quantize": 3, "quantize_delayed": 3, "cast_transpose": 4, "amax": 2,
@@ -360,6 +368,8 @@ def run_ours(args, rank, world):
                      "traffic": traffic, "algorithmic_bytes_per_launch": round(alg_per_launch)},
         "kernels": kernels,
         "variants": variants,
+        "kernel_timing": f"CUDA events around every launch on the launching stream, {ksteps} steps right after "
+                         f"the timed region (the timed region itself carries no per-launch events)",
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -24,7 +24,8 @@ FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 __all__ = [
     "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
     "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
-    "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_amax_noalloc", "launch_count", "version", "library",
+    "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_quantize_mx", "fp8_dequantize_mx",
+    "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "launch_count", "version", "library",
 ]
 
 
@@ -93,6 +94,39 @@ def fp8_amax(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None
     """amax_out[0] = max|x|; with scale_out / scale_inv_out, also the current scale."""
     _check(library().fp8_amax(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
                               _p(scale_out), _p(scale_inv_out), _stream(stream)))
+
+
+def fp8_quantize_mx(x, fmt, q_row=None, scale_row=None, q_col=None, scale_col=None, stream=None):
+    """MXFP8: codes with one E8M0 scale per 32 elements, rowwise ([rows, cols] codes,
+    [rows, ceil(cols/32)] scales) and/or columnwise (transposed: [cols, rows] codes,
+    [cols, ceil(rows/32)] scales)."""
+    rows, cols = _rows_cols(x)
+    for t, shape in ((q_row, (rows, cols)), (scale_row, (rows, -(-cols // 32))), (q_col, (cols, rows)),
+                     (scale_col, (cols, -(-rows // 32)))):
+        if t is not None and (t.dtype != torch.uint8 or tuple(t.shape) != shape):
+            raise ValueError(f"MX outputs must be uint8 {shape}")
+    _check(library().fp8_quantize_mx(_p(x), _dt(x), rows, cols, fmt, _p(q_row), _p(scale_row), _p(q_col),
+                                     _p(scale_col), _stream(stream)))
+
+
+def fp8_dequantize_mx(q, scales, fmt, y, stream=None):
+    """y = decode(q) * 2^(scale - 127) for rowwise MX data [rows, cols]."""
+    rows, cols = _rows_cols(q)
+    if scales.dtype != torch.uint8 or tuple(scales.shape) != (rows, -(-cols // 32)):
+        raise ValueError("scales must be uint8 [rows, ceil(cols/32)]")
+    if tuple(y.shape) != (rows, cols):
+        raise ValueError("y must have q's shape")
+    _check(library().fp8_dequantize_mx(_p(q), _p(scales), fmt, rows, cols, _p(y), _dt(y), _stream(stream)))
+
+
+def fp8_block128_scales_to_mx(scale_inv, rows, cols, mx_scales, bad_blocks_out=None, stream=None):
+    """E8M0 1x32 scales from power-of-two 128x128 block scale_inv (codes unchanged)."""
+    if scale_inv.dtype != torch.float32 or mx_scales.dtype != torch.uint8:
+        raise TypeError("scale_inv must be float32 and mx_scales uint8")
+    if tuple(mx_scales.shape) != (rows, -(-cols // 32)):
+        raise ValueError("mx_scales must be uint8 [rows, ceil(cols/32)]")
+    _check(library().fp8_block128_scales_to_mx(_p(scale_inv), rows, cols, _p(mx_scales), _p(bad_blocks_out),
+                                               _stream(stream)))
 
 
 def fp8_amax_noalloc(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):

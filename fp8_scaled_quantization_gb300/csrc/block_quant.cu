@@ -11,8 +11,8 @@
 // then converted with that block's scale (3 bytes of HBM traffic per element
 // plus 4 bytes per block).
 //   128 x 128: one CTA of 256 threads per block, 64 elements per thread.
-//   1 x 128:   one half-warp per tile, 8 elements per lane, four tiles in
-//              flight per half-warp; the four scales are computed one per
+//   1 x 128:   one half-warp per tile, 8 elements per lane, eight tiles in
+//              flight per half-warp; the eight scales are computed one per
 //              lane and shuffled back, so each lane does one division.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
@@ -101,7 +101,7 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
 
 // ------------------------------------------------------------------ 1 x 128
 
-constexpr int kTilesInFlight = 4;  // per half-warp
+constexpr int kTilesInFlight = 8;  // per half-warp: 8 independent 16-byte loads per lane
 
 // Fast path: cols % 128 == 0, x and q 16-byte aligned, BF16 input; the tiles
 // are then the consecutive 128-element segments of the flat array.
@@ -130,7 +130,7 @@ row128_bf16_kernel(const uint8_t* __restrict__ x, int64_t ntiles, uint8_t* __res
             for (int o = 8; o > 0; o >>= 1) b = umax(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
             amx[k] = b;
         }
-        // Lane l16 < 4 of each half-warp derives the scale of tile k = l16.
+        // Lane l16 < kTilesInFlight of each half-warp derives the scale of tile k = l16.
         uint32_t mine = amx[0];
 #pragma unroll
         for (int k = 1; k < kTilesInFlight; ++k) mine = (l16 == k) ? amx[k] : mine;
@@ -203,10 +203,10 @@ void launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, int b
     }
     const int64_t cap = (int64_t)sm_count() * 8;
     if (bf16 && cols % 128 == 0 && aligned16(x) && aligned16(q)) {
+        // one chunk of kTilesPerCta tiles per CTA (the loop in the kernel runs once)
         const int64_t ntiles = rows * nbc;
         constexpr int kTilesPerCta = (kThreads / 16) * kTilesInFlight;
-        int64_t grid = (ntiles + kTilesPerCta - 1) / kTilesPerCta;
-        if (grid > cap) grid = cap;
+        const int64_t grid = (ntiles + kTilesPerCta - 1) / kTilesPerCta;
         row128_bf16_kernel<FMT><<<(unsigned)grid, kThreads, 0, st>>>(x, ntiles, q, si);
         return;
     }
@@ -236,6 +236,7 @@ extern "C" fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int
     if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
     if (reinterpret_cast<uintptr_t>(scale_inv_out) % 4) return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv_out not 4-byte aligned", fn);
     if (block_rows == 128 && (rows + 127) / 128 > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: rows too large", fn);
+    if (rows * ((cols + 127) / 128) / 16 > 0x7FFFFFFFLL) return fail(FP8_ERR_UNSUPPORTED, "%s: too many tiles", fn);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint8_t* xp = static_cast<const uint8_t*>(x);

@@ -50,7 +50,10 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
                       FinishArgs fa) {
     __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
     const float scale = __ldg(scale_ptr);
-    const int64_t r0 = (int64_t)blockIdx.y * kTile, c0 = (int64_t)blockIdx.x * kTile;
+    // Tiles run in reverse order with evict_first loads: after an amax pass over
+    // x (current scaling) the end of x is the part still in L2.
+    const int64_t r0 = (int64_t)(gridDim.y - 1 - blockIdx.y) * kTile, c0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * kTile;
+    const uint64_t pol = l2_policy_evict_first();
     const int t = threadIdx.x;
     uint32_t am = 0;  // fp32 bits of max |x| seen by this thread
 
@@ -62,7 +65,7 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
             const uint8_t* src = x + ((r0 + rsub) * cols + c0 + cc * 8) * 2;
             uint4 v[8];
 #pragma unroll
-            for (int p = 0; p < 8; ++p) v[p] = ldg_stream(src + (int64_t)p * 16 * cols * 2);
+            for (int p = 0; p < 8; ++p) v[p] = ldg_stream_hint(src + (int64_t)p * 16 * cols * 2, pol);
             uint32_t m16 = 0;
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
@@ -83,7 +86,7 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
             for (int half = 0; half < 2; ++half) {
                 uint4 v[8];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) v[p] = ldg_stream(src + (int64_t)(half * 8 + p) * 8 * cols * 4);
+                for (int p = 0; p < 8; ++p) v[p] = ldg_stream_hint(src + (int64_t)(half * 8 + p) * 8 * cols * 4, pol);
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     float4 f = make_float4(__uint_as_float(v[p].x), __uint_as_float(v[p].y), __uint_as_float(v[p].z),

@@ -259,7 +259,9 @@ struct alignas(64) Workspace {
     unsigned int done;            // CTAs finished in the current launch
     unsigned int amax_bits;       // running max of |x| as fp32 bits
     unsigned long long sat;       // running saturated-element count
-    unsigned int pad[12];
+    unsigned int hist_key;        // delayed recipe: order key of the history max (0 = none)
+    unsigned int hist_nan;        // delayed recipe: a history entry is NaN
+    unsigned int pad[10];
 };
 static_assert(sizeof(Workspace) == 64, "workspace is one 64-byte line");
 
@@ -303,6 +305,27 @@ __device__ __forceinline__ void grid_finish(Workspace* ws, uint32_t cta_amax_bit
 }
 
 // ------------------------------------------------------------ memory ops
+
+// L2 eviction-priority policies (createpolicy, sm_80+).  Current scaling reads
+// x twice (amax, then the cast); the cast runs right after the amax pass in
+// reverse chunk order, so it starts on the part of x the amax pass touched
+// last (still in L2), and marks its loads evict_first: they are x's last use.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ldg_stream_hint(const void* p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
+    return v;
+}
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;

@@ -1,0 +1,298 @@
+// mx_quant.cu -- MXFP8: FP8 codes with one E8M0 (power-of-two) scale per 32
+// consecutive elements, rowwise (1 x 32 blocks) and columnwise (32 x 1 blocks,
+// written transposed), MX dequantize, and the lossless re-blocking of 128 x 128
+// power-of-two block scales into 1 x 32 E8M0 scales.
+//
+// "Megatron FP8" §10 and §16: 32 consecutive elements share one E8M0 scale
+// (8 exponent bits, no mantissa, no sign, 2^-127 .. 2^127, the OCP MX format);
+// "Low Precision Training and Rollout", "MXFP8 (Blackwell only)": E4M3 values
+// with UE8M0 scales per 32-element group, and [128,128] block-FP8 scales
+// rescaled to [1,32] without dequantizing when they are powers of two.
+//
+// Scale rule (OCP MX, the reading the library takes): shared_exp =
+// floor(log2(block amax)) - emax_elem (8 for E4M3, 15 for E5M2), clamped to
+// [-127, 127]; an all-zero block takes -127; a block holding Inf or NaN gets
+// the NaN scale 0xFF and NaN codes.  floor(log2(amax)) is the exponent field
+// of the fp32 amax, so no division is needed; codes are
+// cvt.rn.satfinite(fl32(x * 2^-shared_exp)).
+#include "fp8q_device.cuh"
+#include "fp8q_host.h"
+
+namespace fp8q {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileR = 32, kTileC = 128;  // 32 x 128 tile: 4 row blocks per row, 1 column block per column
+
+template <int FMT> struct MxEmax;
+template <> struct MxEmax<kE4M3> { static constexpr int kE = 8; };
+template <> struct MxEmax<kE5M2> { static constexpr int kE = 15; };
+
+// E8M0 code of a finite, non-negative amax (fp32 bits).
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_scale_code(uint32_t amax_bits) {
+    const int e = (int)(amax_bits >> 23);  // biased exponent; 0 for zero / subnormal amax
+    int se = e - 127 - MxEmax<FMT>::kE;
+    if (e == 0 || se < -127) se = -127;
+    return (uint32_t)(se + 127);
+}
+
+// 2^-shared_exp from the code (exact; -shared_exp lies in [-119, 127]).
+__device__ __forceinline__ float mx_multiplier(uint32_t code) { return exp2i(127 - (int)code); }
+
+// One block's worth of 8 BF16 values -> 8 codes with the block's multiplier.
+template <int FMT>
+__device__ __forceinline__ uint2 mx_codes8(uint4 v, float m) {
+    uint32_t dummy;
+    const Codes8 c = cvt_bf16x8<FMT>(v, m, &dummy);
+    return make_uint2(c.lo, c.hi);
+}
+
+// Fast path: rows % 32 == 0, cols % 128 == 0, BF16, 16-byte aligned pointers.
+// Load: thread t takes 16 bytes (8 elements) of row t / 16 (+16 on the second
+// pass); the 4 lanes of a 32-element row block reduce its amax by shuffles.
+// The BF16 tile is staged in shared memory (rows padded by 4 bytes) for the
+// columnwise pass, where 2 threads share a column's 32 rows.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
+               uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+    constexpr int kPad = kTileC + 2;  // row stride in BF16 elements (65 words: conflict-free column reads)
+    __shared__ __align__(16) uint16_t tile[kTileR * kPad];
+    const int64_t r0 = (int64_t)blockIdx.y * kTileR, c0 = (int64_t)blockIdx.x * kTileC;
+    const int t = threadIdx.x, lane = t & 31;
+    const int cc = t & 15, rsub = t >> 4;  // 16 threads per 256-byte row
+    uint4 v[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) v[p] = ldg_stream(x + ((r0 + p * 16 + rsub) * cols + c0 + cc * 8) * 2);
+    const int64_t nbr = cols / 32;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int r = p * 16 + rsub;
+        uint32_t m16 = max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
+                                 max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w)));
+        uint32_t bits = fold_u16x2_to_f32bits(m16);
+        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
+        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // 4 lanes = one 32-element block
+        uint2 codes;
+        uint32_t code;
+        if (bits >= 0x7F800000u) {
+            code = 0xFFu;
+            codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+            code = mx_scale_code<FMT>(bits);
+            codes = mx_codes8<FMT>(v[p], mx_multiplier(code));
+        }
+        if (q_row) {
+            stg_stream(q_row + (r0 + r) * cols + c0 + cc * 8, codes);
+            if ((lane & 3) == 0) s_row[(r0 + r) * nbr + (c0 >> 5) + (cc >> 2)] = (uint8_t)code;
+        }
+        if (q_col) {
+            uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[r * kPad + cc * 8]);  // 4-byte aligned (kPad even)
+            dst[0] = v[p].x;
+            dst[1] = v[p].y;
+            dst[2] = v[p].z;
+            dst[3] = v[p].w;
+        }
+    }
+    if (!q_col) return;
+    __syncthreads();
+    // Column pass: thread t owns column c = t / 2, rows 16 * (t % 2) .. +15.
+    const int c = t >> 1, h = t & 1;
+    uint32_t hv[8];  // 16 BF16 values of this thread, as pairs
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = tile[(h * 16 + 2 * i) * kPad + c], b = tile[(h * 16 + 2 * i + 1) * kPad + c];
+        hv[i] = a | (b << 16);
+        m = max_u16x2(m, abs_bf16x2(hv[i]));
+    }
+    uint32_t bits = fold_u16x2_to_f32bits(m);
+    bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));  // the two halves of the column block
+    uint4 out;
+    uint32_t code;
+    if (bits >= 0x7F800000u) {
+        code = 0xFFu;
+        out = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+        code = mx_scale_code<FMT>(bits);
+        const float mul = mx_multiplier(code);
+        const uint2 lo = mx_codes8<FMT>(make_uint4(hv[0], hv[1], hv[2], hv[3]), mul);
+        const uint2 hi = mx_codes8<FMT>(make_uint4(hv[4], hv[5], hv[6], hv[7]), mul);
+        out = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    stg_stream(q_col + (c0 + c) * rows + r0 + h * 16, out);
+    if (h == 0) s_col[(c0 + c) * (rows / 32) + (r0 >> 5)] = (uint8_t)code;
+}
+
+// Guarded path for any shape / dtype / alignment: one thread per block.
+template <int FMT, bool BF16>
+__device__ __forceinline__ float mx_load(const uint8_t* x, int64_t e) {
+    if constexpr (BF16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16);
+    else return reinterpret_cast<const float*>(x)[e];
+}
+
+// Blocks of 32 consecutive elements along a line; `stride` is the distance
+// between the block's consecutive elements in x, `nlines` lines of `len`
+// elements.  Output codes go to q[line * len + i], scales to s[line * nb + b].
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+mx_guarded_kernel(const uint8_t* __restrict__ x, int64_t nlines, int64_t len, int64_t line_stride,
+                  int64_t elem_stride, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+    const int64_t nb = (len + 31) / 32;
+    for (int64_t task = (int64_t)blockIdx.x * kThreads + threadIdx.x; task < nlines * nb;
+         task += (int64_t)gridDim.x * kThreads) {
+        const int64_t line = task / nb, b = task % nb;
+        const int64_t i0 = b * 32, i1 = i0 + 32 < len ? i0 + 32 : len;
+        uint32_t bits = 0;
+        for (int64_t i = i0; i < i1; ++i)
+            bits = umax(bits, __float_as_uint(mx_load<FMT, BF16>(x, line * line_stride + i * elem_stride)) & 0x7FFFFFFFu);
+        uint32_t code = bits >= 0x7F800000u ? 0xFFu : mx_scale_code<FMT>(bits);
+        const float mul = mx_multiplier(code);
+        for (int64_t i = i0; i < i1; ++i) {
+            uint32_t c = kNaNCode;
+            if (code != 0xFFu) {
+                uint32_t sat;
+                c = quant_one<FMT>(mx_load<FMT, BF16>(x, line * line_stride + i * elem_stride), mul, &sat);
+            }
+            q[line * len + i] = (uint8_t)c;
+        }
+        s[line * nb + b] = (uint8_t)code;
+    }
+}
+
+// MX dequantize (rowwise layout [rows, cols], scales [rows, ceil(cols / 32)]).
+template <int FMT, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads)
+mx_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
+                  uint8_t* __restrict__ y) {
+    const int64_t nb = (cols + 31) / 32;
+    const int64_t n = rows * cols;
+    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < n; e += (int64_t)gridDim.x * kThreads) {
+        const int64_t r = e / cols, c = e % cols;
+        const uint32_t code = s[r * nb + c / 32];
+        const uint32_t h2 = fp8x2_to_f16x2<FMT>(q[e]);
+        // 2^(code - 127): code 0 is the fp32 subnormal 2^-127; a NaN scale (0xFF) makes the block NaN
+        const float m = code == 0xFFu ? __uint_as_float(0x7FFFFFFFu)
+                                      : (code == 0u ? __uint_as_float(0x00400000u) : exp2i((int)code - 127));
+        const float out = __fmul_rn(f16_lo_to_f32(h2), m);
+        if constexpr (OUT_BF16) reinterpret_cast<uint16_t*>(y)[e] = (uint16_t)(f32x2_to_bf16x2(out, 0.0f) & 0xFFFFu);
+        else reinterpret_cast<float*>(y)[e] = isnan(out) ? __uint_as_float(0x7FFFFFFFu) : out;
+    }
+}
+
+// 128 x 128 scale_inv -> 1 x 32 E8M0 codes; counts blocks whose scale_inv is
+// not a power of two in [2^-127, 2^127] (they get 0xFF).
+__global__ void __launch_bounds__(kThreads)
+block128_to_mx_kernel(const float* __restrict__ si, int64_t rows, int64_t cols, uint8_t* __restrict__ out,
+                      unsigned long long* bad) {
+    const int64_t nb32 = (cols + 31) / 32, nbc128 = (cols + 127) / 128;
+    const int64_t n = rows * nb32;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < n; k += (int64_t)gridDim.x * kThreads) {
+        const int64_t r = k / nb32, b = k % nb32;
+        const uint32_t u = __float_as_uint(si[(r >> 7) * nbc128 + ((b * 32) >> 7)]);
+        uint32_t code = 0xFFu;
+        const uint32_t e = u >> 23, mant = u & 0x7FFFFFu;
+        if (!(u & 0x80000000u) && e >= 1 && e <= 254 && mant == 0) code = e;          // 2^(e-127), e in [1, 254]
+        else if (u == 0x00400000u) code = 0;                                           // 2^-127 (subnormal)
+        out[k] = (uint8_t)code;
+        // count each 128 x 128 block once: at its first row and first 1 x 32 block
+        if (code == 0xFFu && bad && (r & 127) == 0 && ((b * 32) & 127) == 0) atomicAdd(bad, 1ull);
+    }
+}
+
+template <int FMT>
+void launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, uint8_t* q_row, uint8_t* s_row,
+               uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
+    const bool fast = bf16 && rows % kTileR == 0 && cols % kTileC == 0 && aligned16(x) &&
+                      (!q_row || aligned16(q_row)) && (!q_col || aligned16(q_col)) && rows / kTileR <= 65535;
+    if (fast) {
+        dim3 grid((unsigned)(cols / kTileC), (unsigned)(rows / kTileR));
+        if (q_row || q_col) mx_tile_kernel<FMT><<<grid, kThreads, 0, st>>>(x, rows, cols, q_row, s_row, q_col, s_col);
+        return;
+    }
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (q_row) {
+        int64_t g = (rows * ((cols + 31) / 32) + kThreads - 1) / kThreads;
+        g = g < 1 ? 1 : (g > cap ? cap : g);
+        if (bf16) mx_guarded_kernel<FMT, true><<<(unsigned)g, kThreads, 0, st>>>(x, rows, cols, cols, 1, q_row, s_row);
+        else mx_guarded_kernel<FMT, false><<<(unsigned)g, kThreads, 0, st>>>(x, rows, cols, cols, 1, q_row, s_row);
+    }
+    if (q_col) {
+        int64_t g = (cols * ((rows + 31) / 32) + kThreads - 1) / kThreads;
+        g = g < 1 ? 1 : (g > cap ? cap : g);
+        if (bf16) mx_guarded_kernel<FMT, true><<<(unsigned)g, kThreads, 0, st>>>(x, cols, rows, 1, cols, q_col, s_col);
+        else mx_guarded_kernel<FMT, false><<<(unsigned)g, kThreads, 0, st>>>(x, cols, rows, 1, cols, q_col, s_col);
+    }
+}
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8_status_t fp8_quantize_mx(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
+                                        fp8_format_t fmt, uint8_t* q_row, uint8_t* scale_row, uint8_t* q_col,
+                                        uint8_t* scale_col, void* stream) {
+    const char* fn = "fp8_quantize_mx";
+    if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", fn, (int)fmt);
+    if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
+    if ((q_row == nullptr) != (scale_row == nullptr) || (q_col == nullptr) != (scale_col == nullptr))
+        return fail(FP8_ERR_INVALID_ARG, "%s: each direction needs both its codes and its scales", fn);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (x == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: x is NULL", fn);
+    if (q_row == nullptr && q_col == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output requested", fn);
+    if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* xp = static_cast<const uint8_t*>(x);
+    const bool bf16 = dtype == FP8_DT_BF16;
+    if (fmt == FP8_E4M3) launch_mx<kE4M3>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
+    else launch_mx<kE5M2>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
+    return after_launch(fn);
+}
+
+extern "C" fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scales, fp8_format_t fmt, int64_t rows,
+                                          int64_t cols, void* y, fp8_dtype_t out_dtype, void* stream) {
+    const char* fn = "fp8_dequantize_mx";
+    if (!valid_fmt(fmt)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", fn, (int)fmt);
+    if (!valid_dtype(out_dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown out_dtype %d", fn, (int)out_dtype);
+    if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (q == nullptr || scales == nullptr || y == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if (reinterpret_cast<uintptr_t>(y) % dtype_size(out_dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: y not element-aligned", fn);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t g = (rows * cols + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    g = g > cap ? cap : g;
+    uint8_t* yp = static_cast<uint8_t*>(y);
+    const bool bf16 = out_dtype == FP8_DT_BF16;
+    if (fmt == FP8_E4M3) {
+        if (bf16) mx_dequant_kernel<kE4M3, true><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
+        else mx_dequant_kernel<kE4M3, false><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
+    } else {
+        if (bf16) mx_dequant_kernel<kE5M2, true><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
+        else mx_dequant_kernel<kE5M2, false><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
+    }
+    return after_launch(fn);
+}
+
+extern "C" fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t cols,
+                                                  uint8_t* mx_scales, unsigned long long* bad_blocks_out,
+                                                  void* stream) {
+    const char* fn = "fp8_block128_scales_to_mx";
+    if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (scale_inv == nullptr || mx_scales == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if (reinterpret_cast<uintptr_t>(scale_inv) % 4) return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", fn);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (bad_blocks_out) {
+        cudaError_t e = cudaMemsetAsync(bad_blocks_out, 0, sizeof(unsigned long long), st);
+        if (e != cudaSuccess) return cuda_status(e, "fp8_block128_scales_to_mx: cudaMemsetAsync");
+    }
+    int64_t g = (rows * ((cols + 31) / 32) + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    g = g < 1 ? 1 : (g > cap ? cap : g);
+    block128_to_mx_kernel<<<(unsigned)g, kThreads, 0, st>>>(scale_inv, rows, cols, mx_scales, bad_blocks_out);
+    return after_launch(fn);
+}

@@ -25,11 +25,15 @@ template <bool BF16> struct VecCfg {
     static constexpr int64_t kUnitsPerCta = (int64_t)kThreads * kUnits;
 };
 
-// The delayed recipe's history update, done by the last CTA of the cast
-// ("Megatron FP8" §5, update_fp8_meta): write this step's amax into slot
-// step % len, take the window maximum (NaN-propagating) or the slot, and
-// overwrite scale / scale_inv with the scale of the next step.  Every CTA has
-// read the old scale before it arrives, so the overwrite races with nothing.
+// The delayed recipe's history update ("Megatron FP8" §5, update_fp8_meta):
+// write this step's amax into slot step % len, take the window maximum
+// (NaN-propagating) or the slot, and overwrite scale / scale_inv with the
+// scale of the next step.  The window maximum is max(this amax, the maximum
+// of the other len - 1 entries); CTAs b < ceil(len / blockDim) each reduce
+// grid-strided slices of those entries before they arrive, folding an order-preserving
+// key into the workspace, so the last CTA only combines scalars.  Every CTA
+// has read the old scale before it arrives, so the overwrite races with
+// nothing, and no CTA reads the history slot that the last CTA writes.
 struct DelayedArgs {
     float* hist;
     int len;
@@ -39,75 +43,90 @@ struct DelayedArgs {
     float* scale_inv;
 };
 
+// Unsigned key with the order of the float values (NaN handled apart).
+__device__ __forceinline__ uint32_t f32_order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float f32_from_order_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int FMT>
 __device__ __forceinline__ void delayed_finish(Workspace* ws, uint32_t cta_amax_bits, unsigned long long cta_sat,
                                                const FinishArgs& fa, const DelayedArgs& da) {
-    __shared__ int s_last;
-    __shared__ float s_red[32];
-    if (threadIdx.x == 0) {
-        if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
-        if (cta_sat) atomicAdd(&ws->sat, cta_sat);
-        __threadfence();
-        s_last = atomicAdd(&ws->done, 1u) == gridDim.x * gridDim.y * gridDim.z - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) {
-        uint32_t bits = atomicExch(&ws->amax_bits, 0u);
-        const unsigned long long sat = atomicExch(&ws->sat, 0ull);
-        atomicExch(&ws->done, 0u);
-        if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
-        const float amax = __uint_as_float(bits);
-        if (fa.amax_out) *fa.amax_out = amax;
-        if (fa.sat_out) *fa.sat_out = sat;
-        da.hist[da.slot] = amax;
-    }
-    __syncthreads();  // the slot write is visible to the whole CTA
-    float eff;
-    if (da.algo == FP8_AMAX_MOST_RECENT) {
-        eff = da.hist[da.slot];
-    } else {
-        float m = -INFINITY;
-        int saw_nan = 0;
-        for (int i = threadIdx.x; i < da.len; i += blockDim.x) {
+    __shared__ uint32_t s_key[32];
+    const unsigned cta = blockIdx.x;
+    uint32_t key = 0;
+    int nan = 0;
+    const bool scans = da.algo == FP8_AMAX_MAX && (int64_t)cta * blockDim.x < da.len;
+    if (scans) {
+        // grid-strided, so that a grid smaller than the history still covers it
+        for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < da.len;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            if (i == da.slot) continue;
             const float v = da.hist[i];
-            if (isnan(v)) saw_nan = 1;
-            else m = fmaxf(m, v);
+            if (isnan(v)) nan = 1;
+            else key = umax(key, f32_order_key(v));
         }
-        saw_nan = __syncthreads_or(saw_nan);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (lane == 0) s_red[warp] = m;
+        nan = __syncthreads_or(nan);
+        key = __reduce_max_sync(0xFFFFFFFFu, key);
+        if ((threadIdx.x & 31) == 0) s_key[threadIdx.x >> 5] = key;
         __syncthreads();
-        m = lane < (int)(blockDim.x >> 5) ? s_red[lane] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        eff = saw_nan ? __uint_as_float(0x7FC00000u) : m;
+        key = (threadIdx.x < (blockDim.x >> 5)) ? s_key[threadIdx.x] : 0u;
+        key = __reduce_max_sync(0xFFFFFFFFu, key);
     }
-    if (threadIdx.x == 0) {
-        float sc, si;
-        scale_from_amax<FMT>(eff, fa.margin, &sc, &si);
-        *da.scale = sc;
-        *da.scale_inv = si;
+    if (threadIdx.x != 0) return;
+    if (scans) {
+        if (key) atomicMax(&ws->hist_key, key);
+        if (nan) atomicOr(&ws->hist_nan, 1u);
     }
+    if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
+    if (cta_sat) atomicAdd(&ws->sat, cta_sat);
+    __threadfence();
+    if (atomicAdd(&ws->done, 1u) != gridDim.x * gridDim.y * gridDim.z - 1) return;
+    __threadfence();
+    uint32_t bits = atomicExch(&ws->amax_bits, 0u);
+    const unsigned long long sat = atomicExch(&ws->sat, 0ull);
+    const uint32_t hkey = atomicExch(&ws->hist_key, 0u);
+    const uint32_t hnan = atomicExch(&ws->hist_nan, 0u);
+    atomicExch(&ws->done, 0u);
+    if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
+    const float amax = __uint_as_float(bits);
+    if (fa.amax_out) *fa.amax_out = amax;
+    if (fa.sat_out) *fa.sat_out = sat;
+    da.hist[da.slot] = amax;
+    float eff = amax;
+    if (da.algo == FP8_AMAX_MAX) {
+        if (hnan || isnan(amax)) eff = __uint_as_float(0x7FC00000u);
+        else if (hkey) eff = fmaxf(amax, f32_from_order_key(hkey));
+    }
+    float sc, si;
+    scale_from_amax<FMT>(eff, fa.margin, &sc, &si);
+    *da.scale = sc;
+    *da.scale_inv = si;
 }
 
+// At most 48 registers, so that 5 CTAs (1280 threads, 160 KB of loads in
+// flight) fit on an SM whichever reductions are fused in.
 template <int FMT, bool BF16, bool AMAX, bool SAT, bool DELAYED = false>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
 quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n,
                     const float* scale_ptr, Workspace* ws, FinishArgs fa, DelayedArgs da = DelayedArgs{}) {
     using C = VecCfg<BF16>;
     const int64_t nunits = n / 16;
-    const int64_t ubase = (int64_t)blockIdx.x * C::kUnitsPerCta + threadIdx.x;
+    // Chunks run in reverse order with evict_first loads: after an amax pass
+    // over x (current scaling) the end of x is the part still in L2.
+    const int64_t chunk = (int64_t)(gridDim.x - 1 - blockIdx.x);
+    const int64_t ubase = chunk * C::kUnitsPerCta + threadIdx.x;
+    const uint64_t pol = l2_policy_evict_first();
     uint4 v[C::kUnits][C::kLoads];
 #pragma unroll
     for (int k = 0; k < C::kUnits; ++k) {
         const int64_t u = ubase + (int64_t)k * kThreads;
         if (u < nunits) {
 #pragma unroll
-            for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream(x + u * (BF16 ? 32 : 64) + h * 16);
+            for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream_hint(x + u * (BF16 ? 32 : 64) + h * 16, pol);
         }
     }
     const float scale = *scale_ptr;  // plain load: the delayed variant rewrites it at the end
@@ -144,8 +163,8 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
         }
     }
 
-    // Tail (< 16 elements): the last CTA.
-    if (blockIdx.x == gridDim.x - 1) {
+    // Tail (< 16 elements): the CTA of the last chunk.
+    if (chunk == gridDim.x - 1) {
         for (int64_t i = nunits * 16 + threadIdx.x; i < n; i += kThreads) {
             float xv;
             uint32_t b;

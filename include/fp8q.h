@@ -265,6 +265,51 @@ fp8_status_t fp8_dequantize(const uint8_t* q, fp8_format_t fmt, int64_t rows, in
                             fp8_dtype_t out_dtype, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8: E8M0 scale per 32 elements                                         */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §10 / §16: every 32 consecutive elements share one E8M0
+ * scale (8 exponent bits, no mantissa, no sign: 2^-127 .. 2^127; code 0xFF is
+ * NaN) -- the OCP Microscaling format; "Low Precision Training and Rollout",
+ * "MXFP8 (Blackwell only)": E4M3 values with UE8M0 scales per 32-element group.
+ *
+ * Scale of a block (the OCP MX rule): shared_exp = floor(log2(block amax))
+ * - emax (8 for E4M3, 15 for E5M2), clamped to [-127, 127]; an all-zero
+ * block takes -127; a block holding Inf or NaN gets scale 0xFF and NaN codes
+ * (0x7F).  Codes: RNE-saturating encode of fl32(x * 2^-shared_exp).
+ *
+ *   x          device [rows, cols] of `dtype`, row-major.
+ *   q_row      device uint8[rows, cols] or NULL: 1 x 32 blocks along rows.
+ *   scale_row  device uint8[rows, ceil(cols/32)] (with q_row).
+ *   q_col      device uint8[cols, rows] or NULL: 32 x 1 blocks along
+ *              columns, written transposed (row c of q_col is column c of x).
+ *   scale_col  device uint8[cols, ceil(rows/32)] (with q_col).
+ * rows % 32 == 0, cols % 128 == 0, BF16 and 16-byte aligned pointers take
+ * one tiled launch; other shapes take a guarded path (one launch per
+ * direction). */
+fp8_status_t fp8_quantize_mx(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols, fp8_format_t fmt,
+                             uint8_t* q_row, uint8_t* scale_row, uint8_t* q_col, uint8_t* scale_col,
+                             void* stream);
+
+/* y = decode(q) * 2^(scale - 127) in fp32 (one multiply), then BF16 (RNE) or
+ * fp32; q [rows, cols] with scales [rows, ceil(cols/32)] (rowwise layout; a
+ * columnwise copy is dequantized as its own [cols, rows] matrix).  A NaN scale
+ * makes its block NaN (canonical NaN of the output type).  One launch. */
+fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scales, fp8_format_t fmt, int64_t rows,
+                               int64_t cols, void* y, fp8_dtype_t out_dtype, void* stream);
+
+/* "Low Precision Training and Rollout", "MXFP8 (Blackwell only)": block-FP8
+ * [128,128] data re-blocked to [1,32] without dequantizing when its scales are
+ * powers of two.  The codes stay as they are; this writes the E8M0 scale of
+ * every 1 x 32 block from the fp32 scale_inv of its 128 x 128 block
+ * (scale_inv [ceil(rows/128), ceil(cols/128)] as written by
+ * fp8_quantize_block).  A scale_inv that is not a power of two in
+ * [2^-127, 2^127] cannot be carried: its blocks get 0xFF and, when
+ * bad_blocks_out (device uint64[1]) is given, it receives how many 128 x 128
+ * blocks were like that.  One memset node (bad_blocks_out) + one launch. */
+fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t cols, uint8_t* mx_scales,
+                                       unsigned long long* bad_blocks_out, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* amax without any device allocation                                       */
 /* ------------------------------------------------------------------------ */
 /* The pages have no counterpart to this entry point; it serves callers that
