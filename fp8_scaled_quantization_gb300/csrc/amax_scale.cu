@@ -1,19 +1,20 @@
-// amax_scale.cu -- amax reduction with fused current-scale finalize, and the
-// delayed-scaling history update.
+// amax_scale.cu -- amax reduction, the finalize kernel that turns per-CTA
+// partials into amax / saturation totals / scales, and the delayed-scaling
+// history update.
 //
 // amax ("Megatron FP8" §4: a dedicated reduction kernel producing an fp32
 // scalar; §10: current scaling scans the tensor before the cast).  |x| of
 // BF16 is its bit pattern with the sign cleared; for non-negative floats the
 // unsigned order of the bits is the numeric order and NaN patterns sort above
 // Inf, so an unsigned 16-bit max (two lanes per 32-bit word) is an exact,
-// order-free, NaN-propagating amax.  CTAs fold their maximum into a 64-byte
-// workspace; the last CTA to arrive turns it into amax, scale and scale_inv
-// and resets the workspace, so one launch does the whole current-scaling
-// prologue.
+// order-free, NaN-propagating amax.  Each CTA stores its maximum in its own
+// workspace slot; the finalize kernel (one CTA, launched right after with
+// programmatic dependent launch) reduces the slots and derives the scale.
 //
-// Delayed update ("Megatron FP8" §5, update_fp8_meta): one CTA writes the new
-// amax into slot step % len, takes the window maximum (or the slot, for
-// most_recent) and derives scale / scale_inv for the next cast.
+// Delayed update ("Megatron FP8" §5, update_fp8_meta): write the new amax into
+// slot step % len, take the window maximum (or the slot, for most_recent) and
+// derive scale / scale_inv for the next cast.  Used both stand-alone
+// (fp8_update_scale_delayed) and as the finalize of fp8_quantize_delayed.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -22,30 +23,36 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLoads = 8;  // 16-byte loads in flight per thread; one chunk of 256 * 8 loads per CTA
+constexpr int kFinThreads = 1024;
 
 // x is 16-byte aligned here; `n` counts elements of width 2 (BF16) or 4 from x.
+// CTA b reduces chunks b, b + grid, ... (one chunk unless the tensor needs
+// more chunks than there are partial slots).
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 amax_kernel(const uint8_t* __restrict__ head, int head_n, const uint8_t* __restrict__ x, int64_t n,
-            Workspace* ws, FinishArgs fa) {
+            uint32_t* __restrict__ part_amax) {
+    pdl_begin();
     constexpr int kPer = BF16 ? 8 : 4;  // elements per 16-byte chunk
     const int64_t nchunks = n / kPer;
-    const int64_t cbase = (int64_t)blockIdx.x * kThreads * kLoads + threadIdx.x;
-    uint4 v[kLoads];
-#pragma unroll
-    for (int k = 0; k < kLoads; ++k) {
-        const int64_t c = cbase + (int64_t)k * kThreads;
-        v[k] = c < nchunks ? ldg_stream(x + c * 16) : make_uint4(0, 0, 0, 0);
-    }
+    const int64_t per_cta = (int64_t)kThreads * kLoads;
     uint32_t acc = 0;  // BF16: u16x2 lanes; fp32: f32 bits
+    for (int64_t base = (int64_t)blockIdx.x * per_cta + threadIdx.x; base < nchunks; base += (int64_t)gridDim.x * per_cta) {
+        uint4 v[kLoads];
 #pragma unroll
-    for (int k = 0; k < kLoads; ++k) {
-        if constexpr (BF16) {
-            acc = max_u16x2(acc, max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
-                                           max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w))));
-        } else {
-            acc = umax(acc, umax(umax(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu),
-                                 umax(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu)));
+        for (int k = 0; k < kLoads; ++k) {
+            const int64_t c = base + (int64_t)k * kThreads;
+            v[k] = c < nchunks ? ldg_stream(x + c * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+            if constexpr (BF16) {
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
+                                               max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w))));
+            } else {
+                acc = umax(acc, umax(umax(v[k].x & 0x7FFFFFFFu, v[k].y & 0x7FFFFFFFu),
+                                     umax(v[k].z & 0x7FFFFFFFu, v[k].w & 0x7FFFFFFFu)));
+            }
         }
     }
     uint32_t bits = BF16 ? fold_u16x2_to_f32bits(acc) : acc;
@@ -64,39 +71,77 @@ amax_kernel(const uint8_t* __restrict__ head, int head_n, const uint8_t* __restr
 
     __shared__ uint32_t red[32];
     bits = block_max_u32(bits, red);
-    grid_finish(ws, bits, 0ull, fa);
+    if (threadIdx.x == 0) part_amax[blockIdx.x] = bits;
+}
+
+// NaN-propagating maximum of hist[0..len) by the whole CTA (hist already
+// holds this step's amax in its slot); valid in every thread.
+__device__ __forceinline__ float window_max(const float* hist, int len) {
+    __shared__ float red[32];
+    float m = -INFINITY;
+    int saw_nan = 0;
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+        const float v = hist[i];
+        if (isnan(v)) saw_nan = 1;
+        else m = fmaxf(m, v);
+    }
+    saw_nan = __syncthreads_or(saw_nan);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    return saw_nan ? __uint_as_float(0x7FC00000u) : m;
+}
+
+// One CTA: reduce the partials of the previous launch and write the results.
+template <int FMT>
+__global__ void __launch_bounds__(kFinThreads)
+finalize_kernel(const uint32_t* __restrict__ part_amax, const unsigned long long* __restrict__ part_sat, int nparts,
+                float* amax_out, unsigned long long* sat_out, float* scale_out, float* scale_inv_out, int margin,
+                float* hist, int hist_len, int slot, int algo) {
+    pdl_begin();
+    __shared__ uint32_t red[32];
+    __shared__ unsigned long long red64[32];
+    uint32_t bits = 0;
+    unsigned long long sat = 0;
+    for (int i = threadIdx.x; i < nparts; i += kFinThreads) {
+        if (part_amax) bits = umax(bits, part_amax[i]);
+        if (part_sat) sat += part_sat[i];
+    }
+    bits = block_max_u32(bits, red);
+    if (part_sat) sat = block_sum_u64(sat, red64);
+    if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
+    const float amax = __uint_as_float(bits);
+    if (threadIdx.x == 0) {
+        if (amax_out) *amax_out = amax;
+        if (sat_out) *sat_out = sat;
+    }
+    float eff = amax;
+    if (hist != nullptr) {
+        if (threadIdx.x == 0) hist[slot] = amax;
+        __syncthreads();  // the slot write is visible to the whole CTA
+        if (algo == FP8_AMAX_MAX) eff = window_max(hist, hist_len);
+    }
+    if (threadIdx.x == 0 && scale_out != nullptr) {
+        float s, si;
+        scale_from_amax<FMT>(eff, margin, &s, &si);
+        *scale_out = s;
+        *scale_inv_out = si;
+    }
 }
 
 template <int FMT>
 __global__ void __launch_bounds__(1024)
 update_delayed_kernel(float* hist, int len, int slot, const float* new_amax, int algo, int margin,
                       float* scale_out, float* scale_inv_out) {
+    pdl_begin();
     if (new_amax != nullptr && threadIdx.x == 0) hist[slot] = *new_amax;
     __syncthreads();  // the slot write is visible to the whole CTA
-    float eff;
-    if (algo == FP8_AMAX_MOST_RECENT) {
-        eff = hist[slot];
-    } else {
-        // NaN-propagating maximum over the window.
-        float m = -INFINITY;
-        int saw_nan = 0;
-        for (int i = threadIdx.x; i < len; i += blockDim.x) {
-            float v = hist[i];
-            if (isnan(v)) saw_nan = 1;
-            else m = fmaxf(m, v);
-        }
-        saw_nan = __syncthreads_or(saw_nan);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        __shared__ float red[32];
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        m = lane < (int)(blockDim.x >> 5) ? red[lane] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        eff = saw_nan ? __uint_as_float(0x7FC00000u) : m;
-    }
+    const float eff = algo == FP8_AMAX_MOST_RECENT ? hist[slot] : window_max(hist, len);
     if (threadIdx.x == 0) {
         float s, si;
         scale_from_amax<FMT>(eff, margin, &s, &si);
@@ -106,6 +151,17 @@ update_delayed_kernel(float* hist, int len, int slot, const float* new_amax, int
 }
 
 }  // namespace
+
+fp8_status_t launch_finalize(const FinalizeArgs& a, cudaStream_t st) {
+    if (a.fmt == FP8_E4M3)
+        return launch("finalize", finalize_kernel<kE4M3>, dim3(1), dim3(kFinThreads), st, a.part_amax, a.part_sat,
+                      a.nparts, a.amax_out, a.sat_out, a.scale_out, a.scale_inv_out, a.margin, a.hist, a.hist_len,
+                      a.slot, a.algo);
+    return launch("finalize", finalize_kernel<kE5M2>, dim3(1), dim3(kFinThreads), st, a.part_amax, a.part_sat,
+                  a.nparts, a.amax_out, a.sat_out, a.scale_out, a.scale_inv_out, a.margin, a.hist, a.hist_len, a.slot,
+                  a.algo);
+}
+
 }  // namespace fp8q
 
 using namespace fp8q;
@@ -140,14 +196,24 @@ extern "C" fp8_status_t fp8_amax(const void* x, fp8_dtype_t dtype, int64_t n, fl
     const int64_t chunks = body_n / per;
     int64_t grid = (chunks + (int64_t)kThreads * kLoads - 1) / ((int64_t)kThreads * kLoads);
     if (grid < 1) grid = 1;
-    if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "fp8_amax: n too large");
+    if (grid > kMaxPartials) grid = kMaxPartials;
 
-    FinishArgs fa{amax_out, scale_out, scale_inv_out, nullptr, (int)fmt, margin};
     if (dtype == FP8_DT_BF16)
-        amax_kernel<true><<<(unsigned)grid, kThreads, 0, st>>>(p, (int)head, body, body_n, ws, fa);
+        s = launch("fp8_amax", amax_kernel<true>, dim3((unsigned)grid), dim3(kThreads), st, p, (int)head, body, body_n,
+                   ws->amax);
     else
-        amax_kernel<false><<<(unsigned)grid, kThreads, 0, st>>>(p, (int)head, body, body_n, ws, fa);
-    return after_launch("fp8_amax");
+        s = launch("fp8_amax", amax_kernel<false>, dim3((unsigned)grid), dim3(kThreads), st, p, (int)head, body,
+                   body_n, ws->amax);
+    if (s != FP8_OK) return s;
+    FinalizeArgs fa;
+    fa.part_amax = ws->amax;
+    fa.nparts = (int)grid;
+    fa.amax_out = amax_out;
+    fa.scale_out = scale_out;
+    fa.scale_inv_out = scale_inv_out;
+    fa.fmt = (int)fmt;
+    fa.margin = margin;
+    return launch_finalize(fa, st);
 }
 
 extern "C" fp8_status_t fp8_update_scale_delayed(float* amax_history, int history_len, int64_t step,
@@ -169,10 +235,8 @@ extern "C" fp8_status_t fp8_update_scale_delayed(float* amax_history, int histor
     const int slot = (int)(step % history_len);
     const int threads = history_len >= 1024 ? 1024 : (history_len >= 256 ? 256 : 32);
     if (fmt == FP8_E4M3)
-        update_delayed_kernel<kE4M3><<<1, threads, 0, st>>>(amax_history, history_len, slot, new_amax, (int)algo,
-                                                            margin, scale_out, scale_inv_out);
-    else
-        update_delayed_kernel<kE5M2><<<1, threads, 0, st>>>(amax_history, history_len, slot, new_amax, (int)algo,
-                                                            margin, scale_out, scale_inv_out);
-    return after_launch("fp8_update_scale_delayed");
+        return launch("fp8_update_scale_delayed", update_delayed_kernel<kE4M3>, dim3(1), dim3(threads), st,
+                      amax_history, history_len, slot, new_amax, (int)algo, margin, scale_out, scale_inv_out);
+    return launch("fp8_update_scale_delayed", update_delayed_kernel<kE5M2>, dim3(1), dim3(threads), st, amax_history,
+                  history_len, slot, new_amax, (int)algo, margin, scale_out, scale_inv_out);
 }

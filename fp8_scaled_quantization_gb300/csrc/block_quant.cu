@@ -28,6 +28,7 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
                 float* __restrict__ scale_inv, int64_t nbc, int vec_ok) {
+    pdl_begin();
     __shared__ uint32_t red[32];
     __shared__ float s_scale;
     const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
@@ -109,6 +110,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
 row128_bf16_kernel(const uint8_t* __restrict__ x, int64_t ntiles, uint8_t* __restrict__ q,
                    float* __restrict__ scale_inv) {
+    pdl_begin();
     const int t = threadIdx.x;
     const int hw = t >> 4, l16 = t & 15;
     const int lane = t & 31;
@@ -158,6 +160,8 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 row128_guarded_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, int64_t nbc,
                       uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    pdl_begin();
+    pdl_begin();
     const int t = threadIdx.x, hw = t >> 4, l16 = t & 15;
     const int64_t ntiles = rows * nbc;
     for (int64_t tile0 = (int64_t)blockIdx.x * 16; tile0 < ntiles; tile0 += (int64_t)gridDim.x * 16) {
@@ -190,16 +194,16 @@ row128_guarded_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
 }
 
 template <int FMT>
-void launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, int br, uint8_t* q, float* si,
-                  cudaStream_t st) {
+fp8_status_t launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, int br, uint8_t* q, float* si,
+                          cudaStream_t st) {
+    const char* w = "fp8_quantize_block";
     const int64_t nbc = (cols + 127) / 128;
     if (br == 128) {
         const int64_t nbr = (rows + 127) / 128;
         const int vec_ok = aligned16(x) && aligned16(q) && cols % 16 == 0;
-        dim3 grid((unsigned)nbc, (unsigned)nbr);
-        if (bf16) block128_kernel<FMT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, q, si, nbc, vec_ok);
-        else block128_kernel<FMT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, q, si, nbc, vec_ok);
-        return;
+        const dim3 grid((unsigned)nbc, (unsigned)nbr);
+        if (bf16) return launch(w, block128_kernel<FMT, true>, grid, dim3(kThreads), st, x, rows, cols, q, si, nbc, vec_ok);
+        return launch(w, block128_kernel<FMT, false>, grid, dim3(kThreads), st, x, rows, cols, q, si, nbc, vec_ok);
     }
     const int64_t cap = (int64_t)sm_count() * 8;
     if (bf16 && cols % 128 == 0 && aligned16(x) && aligned16(q)) {
@@ -207,13 +211,12 @@ void launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, int b
         const int64_t ntiles = rows * nbc;
         constexpr int kTilesPerCta = (kThreads / 16) * kTilesInFlight;
         const int64_t grid = (ntiles + kTilesPerCta - 1) / kTilesPerCta;
-        row128_bf16_kernel<FMT><<<(unsigned)grid, kThreads, 0, st>>>(x, ntiles, q, si);
-        return;
+        return launch(w, row128_bf16_kernel<FMT>, dim3((unsigned)grid), dim3(kThreads), st, x, ntiles, q, si);
     }
     int64_t grid = (rows * nbc + 15) / 16;
     if (grid > cap) grid = cap;
-    if (bf16) row128_guarded_kernel<FMT, true><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, nbc, q, si);
-    else row128_guarded_kernel<FMT, false><<<(unsigned)grid, kThreads, 0, st>>>(x, rows, cols, nbc, q, si);
+    if (bf16) return launch(w, row128_guarded_kernel<FMT, true>, dim3((unsigned)grid), dim3(kThreads), st, x, rows, cols, nbc, q, si);
+    return launch(w, row128_guarded_kernel<FMT, false>, dim3((unsigned)grid), dim3(kThreads), st, x, rows, cols, nbc, q, si);
 }
 
 }  // namespace
@@ -241,7 +244,6 @@ extern "C" fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint8_t* xp = static_cast<const uint8_t*>(x);
     const bool bf16 = dtype == FP8_DT_BF16;
-    if (fmt == FP8_E4M3) launch_block<kE4M3>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
-    else launch_block<kE5M2>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
-    return after_launch(fn);
+    if (fmt == FP8_E4M3) return launch_block<kE4M3>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
+    return launch_block<kE5M2>(xp, bf16, rows, cols, block_rows, q_out, scale_inv_out, st);
 }

@@ -46,8 +46,9 @@ __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t 
 template <int FMT, bool BF16, bool AMAX>
 __global__ void __launch_bounds__(kThreads)
 cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ scale_ptr,
-                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ q_col, int vec_ok, Workspace* ws,
-                      FinishArgs fa) {
+                      uint8_t* __restrict__ q_row, uint8_t* __restrict__ q_col, int vec_ok,
+                      uint32_t* __restrict__ part_amax) {
+    pdl_begin();
     __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
     const float scale = __ldg(scale_ptr);
     // Tiles run in reverse order with evict_first loads: after an amax pass over
@@ -158,17 +159,19 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
     if constexpr (AMAX) {
         __shared__ uint32_t red[32];
         const uint32_t bits = block_max_u32(am, red);
-        grid_finish(ws, bits, 0ull, fa);
+        if (threadIdx.x == 0) part_amax[blockIdx.y * gridDim.x + blockIdx.x] = bits;
     }
 }
 
 template <int FMT, bool BF16>
-void launch(bool amax, dim3 grid, cudaStream_t st, const uint8_t* x, int64_t rows, int64_t cols, const float* scale,
-            uint8_t* q_row, uint8_t* q_col, int vec_ok, Workspace* ws, const FinishArgs& fa) {
+fp8_status_t launch_ct(bool amax, dim3 grid, cudaStream_t st, const uint8_t* x, int64_t rows, int64_t cols,
+                       const float* scale, uint8_t* q_row, uint8_t* q_col, int vec_ok, uint32_t* pa) {
+    const char* w = "fp8_quantize_cast_transpose";
     if (amax)
-        cast_transpose_kernel<FMT, BF16, true><<<grid, kThreads, 0, st>>>(x, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
-    else
-        cast_transpose_kernel<FMT, BF16, false><<<grid, kThreads, 0, st>>>(x, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
+        return launch(w, cast_transpose_kernel<FMT, BF16, true>, grid, dim3(kThreads), st, x, rows, cols, scale, q_row,
+                      q_col, vec_ok, pa);
+    return launch(w, cast_transpose_kernel<FMT, BF16, false>, grid, dim3(kThreads), st, x, rows, cols, scale, q_row,
+                  q_col, vec_ok, pa);
 }
 
 }  // namespace
@@ -200,22 +203,30 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
         ws = stream_workspace(st, &s);
         if (!ws) return s;
     }
-    FinishArgs fa{amax_out, nullptr, nullptr, nullptr, (int)fmt, 0};
     dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)(gy > 0 ? gy : 1));
     if (n == 0) {
         if (!amax_out) return FP8_OK;
-        grid = dim3(1, 1);  // one guarded CTA with nothing to do but finish the amax
+        grid = dim3(1, 1);  // one guarded CTA with nothing to do but report amax 0
     }
+    if (amax_out && (int64_t)grid.x * grid.y > kMaxPartials)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: the fused amax supports at most %d tiles of 128 x 128", fn, kMaxPartials);
     const int vec_ok = aligned16(x) && (q_row == nullptr || aligned16(q_row)) && (q_col == nullptr || aligned16(q_col)) &&
                        cols % 16 == 0 && rows % 16 == 0;
     const uint8_t* xp = static_cast<const uint8_t*>(x);
     const bool bf16 = dtype == FP8_DT_BF16, am = amax_out != nullptr;
-    if (fmt == FP8_E4M3) {
-        if (bf16) launch<kE4M3, true>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
-        else launch<kE4M3, false>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
-    } else {
-        if (bf16) launch<kE5M2, true>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
-        else launch<kE5M2, false>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, ws, fa);
-    }
-    return after_launch(fn);
+    uint32_t* pa = am ? ws->amax : nullptr;
+    fp8_status_t s;
+    if (fmt == FP8_E4M3)
+        s = bf16 ? launch_ct<kE4M3, true>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, pa)
+                 : launch_ct<kE4M3, false>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, pa);
+    else
+        s = bf16 ? launch_ct<kE5M2, true>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, pa)
+                 : launch_ct<kE5M2, false>(am, grid, st, xp, rows, cols, scale, q_row, q_col, vec_ok, pa);
+    if (s != FP8_OK || !am) return s;
+    FinalizeArgs fa;
+    fa.part_amax = ws->amax;
+    fa.nparts = (int)(grid.x * grid.y);
+    fa.amax_out = amax_out;
+    fa.fmt = (int)fmt;
+    return launch_finalize(fa, st);
 }

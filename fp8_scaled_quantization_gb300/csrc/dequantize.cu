@@ -70,6 +70,7 @@ template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 dequant_tensor_kernel(const uint8_t* __restrict__ q, int64_t n, const float* __restrict__ scale_inv,
                       uint8_t* __restrict__ y) {
+    pdl_begin();
     const int64_t nunits = n / 16;
     const int64_t ubase = (int64_t)blockIdx.x * kThreads * kUnits + threadIdx.x;
     uint4 c[kUnits];
@@ -95,6 +96,7 @@ template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 dequant_rows_kernel(const uint8_t* __restrict__ q, int64_t rows, int64_t cols, const float* __restrict__ scale_inv,
                     int br, int64_t nbc, uint8_t* __restrict__ y, int vec) {
+    pdl_begin();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
         const float* srow = br > 0 ? scale_inv + (br == 1 ? r : (r >> 7)) * nbc : scale_inv;
         if (vec) {
@@ -116,15 +118,15 @@ dequant_rows_kernel(const uint8_t* __restrict__ q, int64_t rows, int64_t cols, c
 }
 
 template <int FMT, bool OUT_BF16>
-void launch(const uint8_t* q, int64_t rows, int64_t cols, const float* si, int br, int bc, uint8_t* y,
-            cudaStream_t st) {
+fp8_status_t launch_deq(const uint8_t* q, int64_t rows, int64_t cols, const float* si, int br, int bc, uint8_t* y,
+                        cudaStream_t st) {
+    const char* w = "fp8_dequantize";
     const int64_t n = rows * cols;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (br == 0 && aligned16(q) && aligned16(y)) {
         int64_t grid = (n / 16 + (int64_t)kThreads * kUnits - 1) / ((int64_t)kThreads * kUnits);
         if (grid < 1) grid = 1;
-        dequant_tensor_kernel<FMT, OUT_BF16><<<(unsigned)grid, kThreads, 0, st>>>(q, n, si, y);
-        return;
+        return launch(w, dequant_tensor_kernel<FMT, OUT_BF16>, dim3((unsigned)grid), dim3(kThreads), st, q, n, si, y);
     }
     const int vec = aligned16(q) && aligned16(y) && cols % 16 == 0;
     const int64_t per_row = vec ? cols / 16 : cols;
@@ -134,7 +136,8 @@ void launch(const uint8_t* q, int64_t rows, int64_t cols, const float* si, int b
     int64_t gy = rows < 65535 ? rows : 65535;
     if (gy < 1) gy = 1;
     const int64_t nbc = bc > 0 ? (cols + bc - 1) / bc : 0;
-    dequant_rows_kernel<FMT, OUT_BF16><<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, st>>>(q, rows, cols, si, br, nbc, y, vec);
+    return launch(w, dequant_rows_kernel<FMT, OUT_BF16>, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), st, q, rows,
+                  cols, si, br, nbc, y, vec);
 }
 
 }  // namespace
@@ -162,12 +165,9 @@ extern "C" fp8_status_t fp8_dequantize(const uint8_t* q, fp8_format_t fmt, int64
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* yp = static_cast<uint8_t*>(y);
     const bool bf16 = out_dtype == FP8_DT_BF16;
-    if (fmt == FP8_E4M3) {
-        if (bf16) launch<kE4M3, true>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
-        else launch<kE4M3, false>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
-    } else {
-        if (bf16) launch<kE5M2, true>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
-        else launch<kE5M2, false>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
-    }
-    return after_launch(fn);
+    if (fmt == FP8_E4M3)
+        return bf16 ? launch_deq<kE4M3, true>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st)
+                    : launch_deq<kE4M3, false>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
+    return bf16 ? launch_deq<kE5M2, true>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st)
+                : launch_deq<kE5M2, false>(q, rows, cols, scale_inv, block_rows, block_cols, yp, st);
 }

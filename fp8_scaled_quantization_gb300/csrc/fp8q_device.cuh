@@ -252,20 +252,30 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
     return v;
 }
 
-// ------------------------------------------------ single-launch grid finish
+// ------------------------------------------------------ reductions across CTAs
 
-// Per-(device, stream) workspace; every launch that uses it leaves it zero.
-struct alignas(64) Workspace {
-    unsigned int done;            // CTAs finished in the current launch
-    unsigned int amax_bits;       // running max of |x| as fp32 bits
-    unsigned long long sat;       // running saturated-element count
-    unsigned int hist_key;        // delayed recipe: order key of the history max (0 = none)
-    unsigned int hist_nan;        // delayed recipe: a history entry is NaN
-    unsigned int pad[10];
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may become resident while the previous kernel on the stream drains.
+// It waits here, before touching any global memory, until that kernel has
+// completed and its writes are visible, then lets its own dependents launch.
+// Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Per-(device, stream) workspace of the reducing casts: each CTA stores its
+// partial max |x| (fp32 bits) and saturated count in its own slot with plain
+// stores -- no atomics or fences, so a CTA retires as soon as its stores are
+// issued -- and a one-CTA finalize kernel launched right after reduces them.
+constexpr int kMaxPartials = 8192;
+struct Workspace {
+    uint32_t amax[kMaxPartials];
+    unsigned long long sat[kMaxPartials];
 };
-static_assert(sizeof(Workspace) == 64, "workspace is one 64-byte line");
 
-// What the last CTA of a launch writes.
+// What a launch that reduced into the workspace leaves to the finalize kernel
+// (kept for the allocation-free amax, which finishes in its last CTA).
 struct FinishArgs {
     float* amax_out;                     // nullable
     float* scale_out;                    // nullable
@@ -274,35 +284,6 @@ struct FinishArgs {
     int fmt;
     int margin;
 };
-
-// Fold this CTA's amax / saturation count into the workspace; the last CTA
-// reads the totals, resets the workspace and writes the outputs.  Called by
-// every thread of every CTA with the CTA-reduced values valid in thread 0.
-// Never waits: the last CTA is the one whose arrival completes the count.
-__device__ __forceinline__ void grid_finish(Workspace* ws, uint32_t cta_amax_bits,
-                                            unsigned long long cta_sat, const FinishArgs& fa) {
-    if (threadIdx.x != 0) return;
-    if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
-    if (cta_sat) atomicAdd(&ws->sat, cta_sat);
-    __threadfence();
-    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
-    const unsigned int prev = atomicAdd(&ws->done, 1u);
-    if (prev != total - 1) return;
-    __threadfence();
-    uint32_t bits = atomicExch(&ws->amax_bits, 0u);
-    unsigned long long sat = atomicExch(&ws->sat, 0ull);
-    atomicExch(&ws->done, 0u);
-    if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
-    const float amax = __uint_as_float(bits);
-    if (fa.amax_out) *fa.amax_out = amax;
-    if (fa.sat_out) *fa.sat_out = sat;
-    if (fa.scale_out) {
-        float si;
-        float s = scale_from_amax_rt(fa.fmt, amax, fa.margin, &si);
-        *fa.scale_out = s;
-        *fa.scale_inv_out = si;
-    }
-}
 
 // ------------------------------------------------------------ memory ops
 

@@ -22,9 +22,50 @@ fp8_status_t after_launch(const char* kernel);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
-// Zero-initialised 64-byte workspace of (current device, stream); nullptr on
+// Workspace of (current device, stream) for per-CTA partials; nullptr on
 // failure (the error message is set).
 Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st);
+
+// Launch `kernel` on `st` with programmatic stream serialization allowed (the
+// kernel starts with pdl_begin()), then check and count the launch.
+template <typename... KArgs, typename... Args>
+fp8_status_t launch(const char* what, void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                    Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) return cuda_status(e, what);
+    return after_launch(what);
+}
+
+// What the one-CTA finalize kernel does with the partials of `nparts` CTAs:
+// amax (NaN-canonical) and saturation totals, the current scale from the amax,
+// or -- when hist is set -- the delayed update (hist[slot] = amax, scale from
+// the window) written to scale_out / scale_inv_out.
+struct FinalizeArgs {
+    const uint32_t* part_amax = nullptr;
+    const unsigned long long* part_sat = nullptr;
+    int nparts = 0;
+    float* amax_out = nullptr;
+    unsigned long long* sat_out = nullptr;
+    float* scale_out = nullptr;
+    float* scale_inv_out = nullptr;
+    int fmt = FP8_E4M3;
+    int margin = 0;
+    float* hist = nullptr;
+    int hist_len = 0;
+    int slot = 0;
+    int algo = FP8_AMAX_MAX;
+};
+fp8_status_t launch_finalize(const FinalizeArgs& fa, cudaStream_t st);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }

@@ -57,6 +57,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
 mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+    pdl_begin();
     constexpr int kPad = kTileC + 2;  // row stride in BF16 elements (65 words: conflict-free column reads)
     __shared__ __align__(16) uint16_t tile[kTileR * kPad];
     const int64_t r0 = (int64_t)blockIdx.y * kTileR, c0 = (int64_t)blockIdx.x * kTileC;
@@ -139,6 +140,7 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 mx_guarded_kernel(const uint8_t* __restrict__ x, int64_t nlines, int64_t len, int64_t line_stride,
                   int64_t elem_stride, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+    pdl_begin();
     const int64_t nb = (len + 31) / 32;
     for (int64_t task = (int64_t)blockIdx.x * kThreads + threadIdx.x; task < nlines * nb;
          task += (int64_t)gridDim.x * kThreads) {
@@ -166,6 +168,7 @@ template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 mx_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t rows, int64_t cols,
                   uint8_t* __restrict__ y) {
+    pdl_begin();
     const int64_t nb = (cols + 31) / 32;
     const int64_t n = rows * cols;
     for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < n; e += (int64_t)gridDim.x * kThreads) {
@@ -186,6 +189,7 @@ mx_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, 
 __global__ void __launch_bounds__(kThreads)
 block128_to_mx_kernel(const float* __restrict__ si, int64_t rows, int64_t cols, uint8_t* __restrict__ out,
                       unsigned long long* bad) {
+    pdl_begin();
     const int64_t nb32 = (cols + 31) / 32, nbc128 = (cols + 127) / 128;
     const int64_t n = rows * nb32;
     for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < n; k += (int64_t)gridDim.x * kThreads) {
@@ -202,28 +206,36 @@ block128_to_mx_kernel(const float* __restrict__ si, int64_t rows, int64_t cols, 
 }
 
 template <int FMT>
-void launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, uint8_t* q_row, uint8_t* s_row,
-               uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
+fp8_status_t launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, uint8_t* q_row, uint8_t* s_row,
+                       uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
+    const char* w = "fp8_quantize_mx";
     const bool fast = bf16 && rows % kTileR == 0 && cols % kTileC == 0 && aligned16(x) &&
                       (!q_row || aligned16(q_row)) && (!q_col || aligned16(q_col)) && rows / kTileR <= 65535;
     if (fast) {
-        dim3 grid((unsigned)(cols / kTileC), (unsigned)(rows / kTileR));
-        if (q_row || q_col) mx_tile_kernel<FMT><<<grid, kThreads, 0, st>>>(x, rows, cols, q_row, s_row, q_col, s_col);
-        return;
+        const dim3 grid((unsigned)(cols / kTileC), (unsigned)(rows / kTileR));
+        return launch(w, mx_tile_kernel<FMT>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col, s_col);
     }
     const int64_t cap = (int64_t)sm_count() * 8;
     if (q_row) {
         int64_t g = (rows * ((cols + 31) / 32) + kThreads - 1) / kThreads;
         g = g < 1 ? 1 : (g > cap ? cap : g);
-        if (bf16) mx_guarded_kernel<FMT, true><<<(unsigned)g, kThreads, 0, st>>>(x, rows, cols, cols, 1, q_row, s_row);
-        else mx_guarded_kernel<FMT, false><<<(unsigned)g, kThreads, 0, st>>>(x, rows, cols, cols, 1, q_row, s_row);
+        const int64_t one = 1;
+        fp8_status_t s = bf16 ? launch(w, mx_guarded_kernel<FMT, true>, dim3((unsigned)g), dim3(kThreads), st, x, rows,
+                                       cols, cols, one, q_row, s_row)
+                              : launch(w, mx_guarded_kernel<FMT, false>, dim3((unsigned)g), dim3(kThreads), st, x, rows,
+                                       cols, cols, one, q_row, s_row);
+        if (s != FP8_OK) return s;
     }
     if (q_col) {
         int64_t g = (cols * ((rows + 31) / 32) + kThreads - 1) / kThreads;
         g = g < 1 ? 1 : (g > cap ? cap : g);
-        if (bf16) mx_guarded_kernel<FMT, true><<<(unsigned)g, kThreads, 0, st>>>(x, cols, rows, 1, cols, q_col, s_col);
-        else mx_guarded_kernel<FMT, false><<<(unsigned)g, kThreads, 0, st>>>(x, cols, rows, 1, cols, q_col, s_col);
+        const int64_t one = 1;
+        return bf16 ? launch(w, mx_guarded_kernel<FMT, true>, dim3((unsigned)g), dim3(kThreads), st, x, cols, rows, one,
+                             cols, q_col, s_col)
+                    : launch(w, mx_guarded_kernel<FMT, false>, dim3((unsigned)g), dim3(kThreads), st, x, cols, rows,
+                             one, cols, q_col, s_col);
     }
+    return FP8_OK;
 }
 
 }  // namespace
@@ -247,9 +259,8 @@ extern "C" fp8_status_t fp8_quantize_mx(const void* x, fp8_dtype_t dtype, int64_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint8_t* xp = static_cast<const uint8_t*>(x);
     const bool bf16 = dtype == FP8_DT_BF16;
-    if (fmt == FP8_E4M3) launch_mx<kE4M3>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
-    else launch_mx<kE5M2>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
-    return after_launch(fn);
+    if (fmt == FP8_E4M3) return launch_mx<kE4M3>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
+    return launch_mx<kE5M2>(xp, bf16, rows, cols, q_row, scale_row, q_col, scale_col, st);
 }
 
 extern "C" fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scales, fp8_format_t fmt, int64_t rows,
@@ -267,14 +278,12 @@ extern "C" fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scale
     g = g > cap ? cap : g;
     uint8_t* yp = static_cast<uint8_t*>(y);
     const bool bf16 = out_dtype == FP8_DT_BF16;
-    if (fmt == FP8_E4M3) {
-        if (bf16) mx_dequant_kernel<kE4M3, true><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
-        else mx_dequant_kernel<kE4M3, false><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
-    } else {
-        if (bf16) mx_dequant_kernel<kE5M2, true><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
-        else mx_dequant_kernel<kE5M2, false><<<(unsigned)g, kThreads, 0, st>>>(q, scales, rows, cols, yp);
-    }
-    return after_launch(fn);
+    const dim3 grid((unsigned)g), block(kThreads);
+    if (fmt == FP8_E4M3)
+        return bf16 ? launch(fn, mx_dequant_kernel<kE4M3, true>, grid, block, st, q, scales, rows, cols, yp)
+                    : launch(fn, mx_dequant_kernel<kE4M3, false>, grid, block, st, q, scales, rows, cols, yp);
+    return bf16 ? launch(fn, mx_dequant_kernel<kE5M2, true>, grid, block, st, q, scales, rows, cols, yp)
+                : launch(fn, mx_dequant_kernel<kE5M2, false>, grid, block, st, q, scales, rows, cols, yp);
 }
 
 extern "C" fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t cols,
@@ -293,6 +302,6 @@ extern "C" fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_
     int64_t g = (rows * ((cols + 31) / 32) + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)sm_count() * 8;
     g = g < 1 ? 1 : (g > cap ? cap : g);
-    block128_to_mx_kernel<<<(unsigned)g, kThreads, 0, st>>>(scale_inv, rows, cols, mx_scales, bad_blocks_out);
-    return after_launch(fn);
+    return launch(fn, block128_to_mx_kernel, dim3((unsigned)g), dim3(kThreads), st, scale_inv, rows, cols, mx_scales,
+                  bad_blocks_out);
 }

@@ -1,13 +1,19 @@
 // quantize.cu -- per-tensor scaled cast BF16/FP32 -> E4M3FN/E5M2 with an
-// optional fused amax (the delayed recipe records it) and saturation count.
+// optional fused amax (the delayed recipe records it) and saturation count,
+// and the fused delayed-scaling step (cast + history update).
 //
 // "Megatron FP8" §4 (x * scale, clamp to +-FP8_MAX), §2 (E4M3FN saturates,
-// E5M2 keeps Inf), §6 (cast_to_fp8 feeding the FP8 GEMM), §24 (overflow
-// counts per layer).
+// E5M2 keeps Inf), §5 (delayed scaling: record amax, update the history, derive
+// the next scale), §6 (cast_to_fp8 feeding the FP8 GEMM), §24 (overflow counts
+// per layer).
 //
 // HBM-bound: each thread moves 16 elements per unit (two 16-byte BF16 loads or
 // four 16-byte fp32 loads in, one 16-byte code store out) and keeps 8 loads in
 // flight; one CTA per fixed chunk of 16384 (BF16) / 8192 (fp32) elements.
+// Chunks run in reverse order with evict_first loads: after an amax pass over
+// x (current scaling) the end of x is the part still in L2.  Reductions store
+// one partial per CTA in the stream workspace (plain stores, so a CTA retires
+// as soon as its stores are issued); the finalize kernel reduces them.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -16,155 +22,72 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// 16-element units per thread: every thread issues all its 16-byte loads
-// (8 for BF16, 8 for fp32) before converting, and each CTA owns one fixed
-// chunk of 256 * kUnits units; the hardware scheduler balances the CTAs.
 template <bool BF16> struct VecCfg {
     static constexpr int kUnits = BF16 ? 4 : 2;
     static constexpr int kLoads = BF16 ? 2 : 4;  // 16-byte loads per unit
     static constexpr int64_t kUnitsPerCta = (int64_t)kThreads * kUnits;
 };
 
-// The delayed recipe's history update ("Megatron FP8" §5, update_fp8_meta):
-// write this step's amax into slot step % len, take the window maximum
-// (NaN-propagating) or the slot, and overwrite scale / scale_inv with the
-// scale of the next step.  The window maximum is max(this amax, the maximum
-// of the other len - 1 entries); CTAs b < ceil(len / blockDim) each reduce
-// grid-strided slices of those entries before they arrive, folding an order-preserving
-// key into the workspace, so the last CTA only combines scalars.  Every CTA
-// has read the old scale before it arrives, so the overwrite races with
-// nothing, and no CTA reads the history slot that the last CTA writes.
-struct DelayedArgs {
-    float* hist;
-    int len;
-    int slot;
-    int algo;
-    float* scale;
-    float* scale_inv;
-};
-
-// Unsigned key with the order of the float values (NaN handled apart).
-__device__ __forceinline__ uint32_t f32_order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float f32_from_order_key(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-template <int FMT>
-__device__ __forceinline__ void delayed_finish(Workspace* ws, uint32_t cta_amax_bits, unsigned long long cta_sat,
-                                               const FinishArgs& fa, const DelayedArgs& da) {
-    __shared__ uint32_t s_key[32];
-    const unsigned cta = blockIdx.x;
-    uint32_t key = 0;
-    int nan = 0;
-    const bool scans = da.algo == FP8_AMAX_MAX && (int64_t)cta * blockDim.x < da.len;
-    if (scans) {
-        // grid-strided, so that a grid smaller than the history still covers it
-        for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < da.len;
-             i += (int64_t)gridDim.x * blockDim.x) {
-            if (i == da.slot) continue;
-            const float v = da.hist[i];
-            if (isnan(v)) nan = 1;
-            else key = umax(key, f32_order_key(v));
-        }
-        nan = __syncthreads_or(nan);
-        key = __reduce_max_sync(0xFFFFFFFFu, key);
-        if ((threadIdx.x & 31) == 0) s_key[threadIdx.x >> 5] = key;
-        __syncthreads();
-        key = (threadIdx.x < (blockDim.x >> 5)) ? s_key[threadIdx.x] : 0u;
-        key = __reduce_max_sync(0xFFFFFFFFu, key);
-    }
-    if (threadIdx.x != 0) return;
-    if (scans) {
-        if (key) atomicMax(&ws->hist_key, key);
-        if (nan) atomicOr(&ws->hist_nan, 1u);
-    }
-    if (cta_amax_bits) atomicMax(&ws->amax_bits, cta_amax_bits);
-    if (cta_sat) atomicAdd(&ws->sat, cta_sat);
-    __threadfence();
-    if (atomicAdd(&ws->done, 1u) != gridDim.x * gridDim.y * gridDim.z - 1) return;
-    __threadfence();
-    uint32_t bits = atomicExch(&ws->amax_bits, 0u);
-    const unsigned long long sat = atomicExch(&ws->sat, 0ull);
-    const uint32_t hkey = atomicExch(&ws->hist_key, 0u);
-    const uint32_t hnan = atomicExch(&ws->hist_nan, 0u);
-    atomicExch(&ws->done, 0u);
-    if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
-    const float amax = __uint_as_float(bits);
-    if (fa.amax_out) *fa.amax_out = amax;
-    if (fa.sat_out) *fa.sat_out = sat;
-    da.hist[da.slot] = amax;
-    float eff = amax;
-    if (da.algo == FP8_AMAX_MAX) {
-        if (hnan || isnan(amax)) eff = __uint_as_float(0x7FC00000u);
-        else if (hkey) eff = fmaxf(amax, f32_from_order_key(hkey));
-    }
-    float sc, si;
-    scale_from_amax<FMT>(eff, fa.margin, &sc, &si);
-    *da.scale = sc;
-    *da.scale_inv = si;
-}
-
 // At most 48 registers, so that 5 CTAs (1280 threads, 160 KB of loads in
 // flight) fit on an SM whichever reductions are fused in.
-template <int FMT, bool BF16, bool AMAX, bool SAT, bool DELAYED = false>
+template <int FMT, bool BF16, bool AMAX, bool SAT>
 __global__ void __launch_bounds__(kThreads, 5)
-quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n,
-                    const float* scale_ptr, Workspace* ws, FinishArgs fa, DelayedArgs da = DelayedArgs{}) {
+quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n, const float* scale_ptr,
+                    uint32_t* __restrict__ part_amax, unsigned long long* __restrict__ part_sat) {
+    pdl_begin();
     using C = VecCfg<BF16>;
     const int64_t nunits = n / 16;
-    // Chunks run in reverse order with evict_first loads: after an amax pass
-    // over x (current scaling) the end of x is the part still in L2.
-    const int64_t chunk = (int64_t)(gridDim.x - 1 - blockIdx.x);
-    const int64_t ubase = chunk * C::kUnitsPerCta + threadIdx.x;
+    const int64_t nchunks = (nunits + C::kUnitsPerCta - 1) / C::kUnitsPerCta;
     const uint64_t pol = l2_policy_evict_first();
-    uint4 v[C::kUnits][C::kLoads];
-#pragma unroll
-    for (int k = 0; k < C::kUnits; ++k) {
-        const int64_t u = ubase + (int64_t)k * kThreads;
-        if (u < nunits) {
-#pragma unroll
-            for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream_hint(x + u * (BF16 ? 32 : 64) + h * 16, pol);
-        }
-    }
-    const float scale = *scale_ptr;  // plain load: the delayed variant rewrites it at the end
+    const float scale = *scale_ptr;
     uint32_t am16 = 0;  // BF16: u16x2 max of |x|
     uint32_t am32 = 0;  // fp32 bits max of |x|
     uint32_t sat = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int64_t chunk = nchunks - 1 - c;  // reverse order
+        const int64_t ubase = chunk * C::kUnitsPerCta + threadIdx.x;
+        uint4 v[C::kUnits][C::kLoads];
 #pragma unroll
-    for (int k = 0; k < C::kUnits; ++k) {
-        const int64_t u = ubase + (int64_t)k * kThreads;
-        if (u >= nunits) break;
-        if constexpr (BF16) {
-            Codes8 c[2];
+        for (int k = 0; k < C::kUnits; ++k) {
+            const int64_t u = ubase + (int64_t)k * kThreads;
+            if (u < nunits) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t m;
-                c[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
-                if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale))
-                    sat += fixup_bf16x8<FMT>(v[k][h], scale, &c[h]);
-                if constexpr (AMAX) am16 = max_u16x2(am16, m);
+                for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream_hint(x + u * (BF16 ? 32 : 64) + h * 16, pol);
             }
-            stg_stream(q + u * 16, make_uint4(c[0].lo, c[0].hi, c[1].lo, c[1].hi));
-        } else {
-            uint32_t w[4];
+        }
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
-                                       __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
-                uint32_t m;
-                w[h] = cvt_f32x4<FMT>(f, scale, &m);
-                if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w[h]);
-                if constexpr (AMAX) am32 = umax(am32, m);
+        for (int k = 0; k < C::kUnits; ++k) {
+            const int64_t u = ubase + (int64_t)k * kThreads;
+            if (u >= nunits) break;
+            if constexpr (BF16) {
+                Codes8 cd[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t m;
+                    cd[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
+                    if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale))
+                        sat += fixup_bf16x8<FMT>(v[k][h], scale, &cd[h]);
+                    if constexpr (AMAX) am16 = max_u16x2(am16, m);
+                }
+                stg_stream(q + u * 16, make_uint4(cd[0].lo, cd[0].hi, cd[1].lo, cd[1].hi));
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
+                                           __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
+                    uint32_t m;
+                    w[h] = cvt_f32x4<FMT>(f, scale, &m);
+                    if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w[h]);
+                    if constexpr (AMAX) am32 = umax(am32, m);
+                }
+                stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
             }
-            stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
         }
     }
 
-    // Tail (< 16 elements): the CTA of the last chunk.
-    if (chunk == gridDim.x - 1) {
+    // Tail (< 16 elements): CTA 0.
+    if (blockIdx.x == 0) {
         for (int64_t i = nunits * 16 + threadIdx.x; i < n; i += kThreads) {
             float xv;
             uint32_t b;
@@ -183,23 +106,26 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
         }
     }
 
-    if constexpr (AMAX || SAT || DELAYED) {
+    if constexpr (AMAX || SAT) {
         __shared__ uint32_t red[32];
         __shared__ unsigned long long red64[32];
         uint32_t bits = umax(am32, BF16 ? fold_u16x2_to_f32bits(am16) : 0u);
-        bits = block_max_u32(bits, red);
-        unsigned long long total = SAT ? block_sum_u64((unsigned long long)sat, red64) : 0ull;
-        if constexpr (DELAYED) delayed_finish<FMT>(ws, bits, total, fa, da);
-        else grid_finish(ws, bits, total, fa);
+        if constexpr (AMAX) bits = block_max_u32(bits, red);
+        unsigned long long total = 0;
+        if constexpr (SAT) total = block_sum_u64((unsigned long long)sat, red64);
+        if (threadIdx.x == 0) {
+            if constexpr (AMAX) part_amax[blockIdx.x] = bits;
+            if constexpr (SAT) part_sat[blockIdx.x] = total;
+        }
     }
 }
 
 // Element-at-a-time path for pointers that are not 16-byte aligned.
-template <int FMT, bool BF16, bool DELAYED = false>
+template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
-quantize_scalar_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n,
-                       const float* scale_ptr, Workspace* ws, FinishArgs fa, int reduce,
-                       DelayedArgs da = DelayedArgs{}) {
+quantize_scalar_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n, const float* scale_ptr,
+                       uint32_t* __restrict__ part_amax, unsigned long long* __restrict__ part_sat) {
+    pdl_begin();
     const float scale = *scale_ptr;
     uint32_t am = 0, sat = 0;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
@@ -218,23 +144,61 @@ quantize_scalar_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, i
         sat += s;
         am = umax(am, b);
     }
-    if (reduce || DELAYED) {
+    if (part_amax != nullptr || part_sat != nullptr) {
         __shared__ uint32_t red[32];
         __shared__ unsigned long long red64[32];
-        uint32_t bits = block_max_u32(am, red);
-        unsigned long long total = block_sum_u64((unsigned long long)sat, red64);
-        if constexpr (DELAYED) delayed_finish<FMT>(ws, bits, total, fa, da);
-        else grid_finish(ws, bits, total, fa);
+        const uint32_t bits = block_max_u32(am, red);
+        const unsigned long long total = block_sum_u64((unsigned long long)sat, red64);
+        if (threadIdx.x == 0) {
+            if (part_amax) part_amax[blockIdx.x] = bits;
+            if (part_sat) part_sat[blockIdx.x] = total;
+        }
     }
 }
 
 template <int FMT, bool BF16>
-void launch_vec(bool amax, bool satc, unsigned grid, cudaStream_t st, const uint8_t* x, uint8_t* q, int64_t n,
-                const float* scale, Workspace* ws, const FinishArgs& fa) {
-    if (amax && satc) quantize_vec_kernel<FMT, BF16, true, true><<<grid, kThreads, 0, st>>>(x, q, n, scale, ws, fa);
-    else if (amax) quantize_vec_kernel<FMT, BF16, true, false><<<grid, kThreads, 0, st>>>(x, q, n, scale, ws, fa);
-    else if (satc) quantize_vec_kernel<FMT, BF16, false, true><<<grid, kThreads, 0, st>>>(x, q, n, scale, ws, fa);
-    else quantize_vec_kernel<FMT, BF16, false, false><<<grid, kThreads, 0, st>>>(x, q, n, scale, ws, fa);
+fp8_status_t launch_vec(bool amax, bool satc, unsigned grid, cudaStream_t st, const uint8_t* x, uint8_t* q, int64_t n,
+                        const float* scale, uint32_t* pa, unsigned long long* ps) {
+    const char* w = "fp8_quantize";
+    const dim3 g(grid), b(kThreads);
+    if (amax && satc) return launch(w, quantize_vec_kernel<FMT, BF16, true, true>, g, b, st, x, q, n, scale, pa, ps);
+    if (amax) return launch(w, quantize_vec_kernel<FMT, BF16, true, false>, g, b, st, x, q, n, scale, pa, ps);
+    if (satc) return launch(w, quantize_vec_kernel<FMT, BF16, false, true>, g, b, st, x, q, n, scale, pa, ps);
+    return launch(w, quantize_vec_kernel<FMT, BF16, false, false>, g, b, st, x, q, n, scale, pa, ps);
+}
+
+// The cast, with per-CTA partials when reducing; *nparts receives their count.
+fp8_status_t enqueue_cast(const uint8_t* x, bool bf16, int64_t n, int fmt, const float* scale, uint8_t* q,
+                          Workspace* ws, bool amax, bool satc, cudaStream_t st, int* nparts) {
+    const bool reduce = amax || satc;
+    uint32_t* pa = reduce ? ws->amax : nullptr;
+    unsigned long long* ps = reduce ? ws->sat : nullptr;
+    if (aligned16(x) && aligned16(q)) {
+        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
+        int64_t grid = (n / 16 + per_cta - 1) / per_cta;
+        const int64_t cap = reduce ? kMaxPartials : 0x7FFFFFFF;
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        *nparts = (int)(reduce ? grid : 0);
+        const unsigned g = (unsigned)grid;
+        if (fmt == FP8_E4M3)
+            return bf16 ? launch_vec<kE4M3, true>(amax, satc, g, st, x, q, n, scale, pa, ps)
+                        : launch_vec<kE4M3, false>(amax, satc, g, st, x, q, n, scale, pa, ps);
+        return bf16 ? launch_vec<kE5M2, true>(amax, satc, g, st, x, q, n, scale, pa, ps)
+                    : launch_vec<kE5M2, false>(amax, satc, g, st, x, q, n, scale, pa, ps);
+    }
+    int64_t grid = (n + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    *nparts = (int)(reduce ? grid : 0);
+    const dim3 g((unsigned)grid), b(kThreads);
+    const char* w = "fp8_quantize";
+    if (fmt == FP8_E4M3)
+        return bf16 ? launch(w, quantize_scalar_kernel<kE4M3, true>, g, b, st, x, q, n, scale, pa, ps)
+                    : launch(w, quantize_scalar_kernel<kE4M3, false>, g, b, st, x, q, n, scale, pa, ps);
+    return bf16 ? launch(w, quantize_scalar_kernel<kE5M2, true>, g, b, st, x, q, n, scale, pa, ps)
+                : launch(w, quantize_scalar_kernel<kE5M2, false>, g, b, st, x, q, n, scale, pa, ps);
 }
 
 }  // namespace
@@ -263,39 +227,18 @@ extern "C" fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n
         ws = stream_workspace(st, &s);
         if (!ws) return s;
     }
-    FinishArgs fa{amax_out, nullptr, nullptr, sat_count_out, (int)fmt, 0};
-    const uint8_t* xp = static_cast<const uint8_t*>(x);
-    const bool bf16 = dtype == FP8_DT_BF16;
-
-    if (aligned16(x) && aligned16(q_out)) {
-        const int64_t units = n / 16;
-        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
-        int64_t grid = (units + per_cta - 1) / per_cta;
-        if (grid < 1) grid = 1;
-        if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "fp8_quantize: n too large");
-        const bool am = amax_out != nullptr, sc = sat_count_out != nullptr;
-        if (fmt == FP8_E4M3) {
-            if (bf16) launch_vec<kE4M3, true>(am, sc, (unsigned)grid, st, xp, q_out, n, scale, ws, fa);
-            else launch_vec<kE4M3, false>(am, sc, (unsigned)grid, st, xp, q_out, n, scale, ws, fa);
-        } else {
-            if (bf16) launch_vec<kE5M2, true>(am, sc, (unsigned)grid, st, xp, q_out, n, scale, ws, fa);
-            else launch_vec<kE5M2, false>(am, sc, (unsigned)grid, st, xp, q_out, n, scale, ws, fa);
-        }
-    } else {
-        int64_t grid = (n + kThreads - 1) / kThreads;
-        const int64_t cap = (int64_t)sm_count() * 8;
-        if (grid > cap) grid = cap;
-        if (grid < 1) grid = 1;
-        const int r = reduce ? 1 : 0;
-        if (fmt == FP8_E4M3) {
-            if (bf16) quantize_scalar_kernel<kE4M3, true><<<(unsigned)grid, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, r);
-            else quantize_scalar_kernel<kE4M3, false><<<(unsigned)grid, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, r);
-        } else {
-            if (bf16) quantize_scalar_kernel<kE5M2, true><<<(unsigned)grid, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, r);
-            else quantize_scalar_kernel<kE5M2, false><<<(unsigned)grid, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, r);
-        }
-    }
-    return after_launch("fp8_quantize");
+    int nparts = 0;
+    fp8_status_t s = enqueue_cast(static_cast<const uint8_t*>(x), dtype == FP8_DT_BF16, n, (int)fmt, scale, q_out, ws,
+                                  amax_out != nullptr, sat_count_out != nullptr, st, &nparts);
+    if (s != FP8_OK || !reduce) return s;
+    FinalizeArgs fa;
+    fa.part_amax = amax_out ? ws->amax : nullptr;
+    fa.part_sat = sat_count_out ? ws->sat : nullptr;
+    fa.nparts = nparts;
+    fa.amax_out = amax_out;
+    fa.sat_out = sat_count_out;
+    fa.fmt = (int)fmt;
+    return launch_finalize(fa, st);
 }
 
 extern "C" fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
@@ -320,42 +263,25 @@ extern "C" fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, i
     fp8_status_t s;
     Workspace* ws = stream_workspace(st, &s);
     if (!ws) return s;
-    FinishArgs fa{amax_out, nullptr, nullptr, sat_count_out, (int)fmt, margin};
-    DelayedArgs da{amax_history, history_len, (int)(step % history_len), (int)algo, scale, scale_inv};
-    const uint8_t* xp = static_cast<const uint8_t*>(x);
-    const bool bf16 = dtype == FP8_DT_BF16, sc = sat_count_out != nullptr;
-    if (aligned16(x) && aligned16(q_out)) {
-        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
-        int64_t grid = (n / 16 + per_cta - 1) / per_cta;
-        if (grid < 1) grid = 1;
-        if (grid > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "%s: n too large", fn);
-        const unsigned g = (unsigned)grid;
-#define FP8Q_LAUNCH_DELAYED(F, B)                                                                                  \
-    do {                                                                                                           \
-        if (sc) quantize_vec_kernel<F, B, true, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, da); \
-        else quantize_vec_kernel<F, B, true, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, da);  \
-    } while (0)
-        if (fmt == FP8_E4M3) {
-            if (bf16) FP8Q_LAUNCH_DELAYED(kE4M3, true);
-            else FP8Q_LAUNCH_DELAYED(kE4M3, false);
-        } else {
-            if (bf16) FP8Q_LAUNCH_DELAYED(kE5M2, true);
-            else FP8Q_LAUNCH_DELAYED(kE5M2, false);
-        }
-#undef FP8Q_LAUNCH_DELAYED
-    } else {
-        int64_t grid = (n + kThreads - 1) / kThreads;
-        const int64_t cap = (int64_t)sm_count() * 8;
-        if (grid > cap) grid = cap;
-        if (grid < 1) grid = 1;
-        const unsigned g = (unsigned)grid;
-        if (fmt == FP8_E4M3) {
-            if (bf16) quantize_scalar_kernel<kE4M3, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
-            else quantize_scalar_kernel<kE4M3, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
-        } else {
-            if (bf16) quantize_scalar_kernel<kE5M2, true, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
-            else quantize_scalar_kernel<kE5M2, false, true><<<g, kThreads, 0, st>>>(xp, q_out, n, scale, ws, fa, 1, da);
-        }
-    }
-    return after_launch(fn);
+    int nparts = 0;
+    s = enqueue_cast(static_cast<const uint8_t*>(x), dtype == FP8_DT_BF16, n, (int)fmt, scale, q_out, ws, true,
+                     sat_count_out != nullptr, st, &nparts);
+    if (s != FP8_OK) return s;
+    // The finalize runs after the cast has completed, so it may overwrite the
+    // scale the cast read.
+    FinalizeArgs fa;
+    fa.part_amax = ws->amax;
+    fa.part_sat = sat_count_out ? ws->sat : nullptr;
+    fa.nparts = nparts;
+    fa.amax_out = amax_out;
+    fa.sat_out = sat_count_out;
+    fa.scale_out = scale;
+    fa.scale_inv_out = scale_inv;
+    fa.fmt = (int)fmt;
+    fa.margin = margin;
+    fa.hist = amax_history;
+    fa.hist_len = history_len;
+    fa.slot = (int)(step % history_len);
+    fa.algo = (int)algo;
+    return launch_finalize(fa, st);
 }

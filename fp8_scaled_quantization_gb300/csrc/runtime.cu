@@ -66,9 +66,8 @@ Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st) {
     auto it = g_workspaces.find(key);
     if (it != g_workspaces.end()) return it->second;
     // First use on this stream.  Relax the thread's capture mode so that the
-    // allocation is legal while a stream is being captured; the zeroing is
-    // enqueued on the stream itself, so under capture it becomes a graph node
-    // ordered before the kernel that needs it.
+    // allocation is legal while a stream is being captured.  The partial slots
+    // need no initial value: a launch writes every slot its finalize reads.
     cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
     cudaThreadExchangeStreamCaptureMode(&mode);
     void* p = nullptr;
@@ -76,12 +75,6 @@ Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st) {
     cudaThreadExchangeStreamCaptureMode(&mode);
     if (e != cudaSuccess) {
         *st = cuda_status(e, "cudaMalloc(workspace)");
-        return nullptr;
-    }
-    e = cudaMemsetAsync(p, 0, sizeof(Workspace), stream);
-    if (e != cudaSuccess) {
-        cudaFree(p);
-        *st = cuda_status(e, "cudaMemsetAsync(workspace)");
         return nullptr;
     }
     auto* ws = static_cast<Workspace*>(p);

@@ -13,7 +13,7 @@
  * Memory.   Every tensor and scalar pointer is a DEVICE pointer owned by the
  *           caller (for example a PyTorch allocation).  The library never
  *           frees caller memory and never synchronises the device or a stream.
- *           The one allocation it makes is a 64-byte reduction workspace per
+ *           The one allocation it makes is a 96 KB reduction workspace per
  *           (device, stream) pair, created on the first call that needs it
  *           and kept until process exit (see "Workspace" below).
  * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
@@ -30,15 +30,20 @@
  *           gives the text.  Kernels never trap or assert on the device.
  * Counters. Outputs named *_out (amax, saturation count, scales) are
  *           overwritten, never accumulated into.
- * Workspace. Reductions that finish in a single launch (amax with a fused
- *           scale, fused amax / saturation count) use a 64-byte per-(device,
- *           stream) workspace that every launch leaves zeroed.  Calls on the
- *           same stream are ordered and safe.  Calls on different streams use
- *           different workspaces and are safe.  A CUDA graph captured from a
- *           stream keeps that stream's workspace address: do not replay such a
- *           graph concurrently with other work on the capturing stream.  The
- *           first call on a new stream allocates (cudaMalloc) with the
- *           thread's capture mode relaxed, so it may happen during capture.
+ * Launches. Every kernel is launched with programmatic stream serialization:
+ *           it may become resident while the previous kernel on the stream
+ *           drains, and it waits for that kernel to complete before it touches
+ *           memory, so stream order is kept.
+ * Workspace. Calls that reduce (amax, a fused amax / saturation count, the
+ *           delayed update) store one partial per CTA in a per-(device,
+ *           stream) workspace; a one-CTA finalize kernel launched right after
+ *           the main kernel reduces them.  Calls on the same stream are
+ *           ordered and safe.  Calls on different streams use different
+ *           workspaces and are safe.  A CUDA graph captured from a stream
+ *           keeps that stream's workspace address: do not replay such a graph
+ *           concurrently with other work on the capturing stream.  The first
+ *           call on a new stream allocates (cudaMalloc) with the thread's
+ *           capture mode relaxed, so it may happen during capture.
  *
  * Special values (the same in every cast):
  *   x NaN          -> code 0x7F (canonical NaN, sign dropped)
@@ -113,9 +118,9 @@ unsigned long long fp8_launch_count(void);
  *   fmt, margin used only when scale_out is given; -126 <= margin <= 126.
  *   scale_out, scale_inv_out
  *               device float[1] each, both NULL or both set: the current
- *               scale from this amax (scale rule above), computed in the same
- *               launch by the last CTA to finish.
- * One kernel launch. */
+ *               scale from this amax (scale rule above), computed by the
+ *               finalize kernel.
+ * Two launches: the reduction and the one-CTA finalize. */
 fp8_status_t fp8_amax(const void* x, fp8_dtype_t dtype, int64_t n, float* amax_out,
                       fp8_format_t fmt, int margin, float* scale_out, float* scale_inv_out,
                       void* stream);
@@ -162,9 +167,10 @@ fp8_status_t fp8_update_scale_delayed(float* amax_history, int history_len, int6
  *   q_out          device uint8[n]: the codes.
  *   amax_out       device float[1] or NULL: max|x| of this tensor, fused
  *                  (the delayed recipe records it for the next update).
- *   sat_count_out  device uint64[1] or NULL: number of finite x_i with
+ *  sat_count_out  device uint64[1] or NULL: number of finite x_i with
  *                  |fl32(x_i * scale)| > FP8_MAX.
- * One kernel launch. */
+ * One kernel launch, plus the one-CTA finalize when amax_out or
+ * sat_count_out is given. */
 fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
                           const float* scale, uint8_t* q_out, float* amax_out,
                           unsigned long long* sat_count_out, void* stream);
@@ -189,7 +195,8 @@ fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_forma
  *   amax_out          device float[1] or NULL: this step's amax.
  *   sat_count_out     device uint64[1] or NULL: as in fp8_quantize.
  *   Other arguments as in fp8_quantize / fp8_update_scale_delayed.
- * One kernel launch. */
+ * Two launches: the cast (which records per-CTA amax / counts) and the
+ * one-CTA finalize, which does the history update and writes the scales. */
 fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt,
                                   float* scale, float* scale_inv, uint8_t* q_out, float* amax_history,
                                   int history_len, int64_t step, fp8_amax_algo_t algo, int margin,
@@ -214,7 +221,8 @@ fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, f
  * Current scaling is fp8_amax(.., scale_out, scale_inv_out) followed by this
  * call.  Interior 128x128 tiles take the vector path when cols % 16 == 0,
  * rows % 16 == 0 and the pointers are 16-byte aligned; edge tiles and other
- * shapes take a guarded element path.  One kernel launch. */
+ * shapes take a guarded element path.  One kernel launch, plus the one-CTA
+ * finalize when amax_out is given (then at most 8192 tiles of 128 x 128). */
 fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64_t rows,
                                          int64_t cols, fp8_format_t fmt, const float* scale,
                                          uint8_t* q_row, uint8_t* q_col, float* amax_out,
