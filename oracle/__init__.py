@@ -82,6 +82,8 @@ def lib():
         L.oref_dequantize_mx.restype = None
         L.oref_block128_scales_to_mx.argtypes = [vp, i64, i64, vp]
         L.oref_block128_scales_to_mx.restype = i64
+        L.oref_quantize_hybrid.argtypes = [vp, i32, i64, i64, i32, f32, i32, f32, i32, vp, vp]
+        L.oref_quantize_hybrid.restype = None
         _lib = L
     return _lib
 
@@ -363,3 +365,21 @@ def block128_scales_to_mx(scale_inv: np.ndarray, rows: int, cols: int):
     out = np.empty((rows, -(-cols // MX_BLOCK)), dtype=np.uint8)
     bad = lib().oref_block128_scales_to_mx(_ptr(si), rows, cols, _ptr(out))
     return out, int(bad)
+
+
+# --------------------------------------------------------------------------- hybrid
+
+SRC_ORIGINAL, SRC_ROWWISE_DEQUANTIZED = 0, 1
+
+
+def quantize_hybrid(x: np.ndarray, fmt_row: int, scale_row, fmt_col: int, scale_col, source: int):
+    """Rowwise [rows, cols] codes in fmt_row / scale_row, columnwise [cols, rows] codes in
+    fmt_col / scale_col from x (source 0) or from the BF16-dequantized rowwise value (source 1)."""
+    assert x.ndim == 2
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    q_row = np.empty((rows, cols), dtype=np.uint8)
+    q_col = np.empty((cols, rows), dtype=np.uint8)
+    lib().oref_quantize_hybrid(_ptr(x), _dtype_of(x), rows, cols, fmt_row, float(np.float32(scale_row)), fmt_col,
+                               float(np.float32(scale_col)), source, _ptr(q_row), _ptr(q_col))
+    return q_row, q_col

@@ -561,3 +561,39 @@ int64_t oref_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t
         }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Hybrid per-direction quantization                                         */
+/* ------------------------------------------------------------------------ */
+/* "[Pytorch][Common] Hybrid quantization #2817": the rowwise and columnwise
+ * copies may use different formats and scalings (per-tensor Float8, any
+ * per-direction combination), and the columnwise copy is quantized either
+ * from the original tensor (columnwise_source = original) or from the
+ * dequantized rowwise value (columnwise_source = rowwise_dequantized).
+ * Reading: the dequantized rowwise value is what fp8_dequantize produces --
+ * fl32(decode(q_row) * fl32(1 / scale_row)) rounded to BF16 -- and the
+ * columnwise copy is written transposed [cols, rows], as in cast-transpose. */
+#define OREF_SRC_ORIGINAL 0
+#define OREF_SRC_ROWWISE_DEQUANTIZED 1
+
+void oref_quantize_hybrid(const void* x, int dt, int64_t rows, int64_t cols, int fmt_row, float scale_row,
+                          int fmt_col, float scale_col, int source, uint8_t* q_row, uint8_t* q_col) {
+    fmt_info fr = make_info(fmt_row), fc = make_info(fmt_col);
+    float scale_inv_row = 1.0f / scale_row;
+    int s;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            q_row[r * cols + c] = quantize_element(load_elem(x, dt, r * cols + c), scale_row, &fr, &s);
+    for (int64_t c = 0; c < cols; ++c)
+        for (int64_t r = 0; r < rows; ++r) {
+            float v;
+            if (source == OREF_SRC_ORIGINAL) {
+                v = load_elem(x, dt, r * cols + c);
+            } else {
+                uint8_t code = quantize_element(load_elem(x, dt, r * cols + c), scale_row, &fr, &s);
+                float y = oref_decode(code, fmt_row) * scale_inv_row; /* fp32 multiply */
+                v = oref_bf16_to_f32(oref_f32_to_bf16(y));            /* the BF16 dequantized value */
+            }
+            q_col[c * rows + r] = quantize_element(v, scale_col, &fc, &s);
+        }
+}

@@ -445,3 +445,45 @@ def test_sqnr_soft_check(oracle, fmt):
     y = oracle.dequantize(q, fmt, np.array([si]), out_dt=oracle.FP32).ravel().astype(np.float64)
     sqnr = 10 * np.log10(np.mean(x.astype(np.float64) ** 2) / np.mean((x - y) ** 2))
     assert sqnr > rule  # floating-point grids do at least as well as the uniform rule of thumb
+
+
+# ------------------------------------------------------------------ hybrid
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_hybrid_same_format_original_is_cast_transpose(oracle):
+    rng = np.random.default_rng(21)
+    bits = _bf16(rng.standard_normal((37, 45)) * 20)
+    for fmt in (E4M3, E5M2):
+        s = np.float32(3.5)
+        qr, qc = oracle.quantize_hybrid(bits, fmt, s, fmt, s, oracle.SRC_ORIGINAL)
+        wr, wc = oracle.cast_transpose(bits, fmt, s)
+        assert np.array_equal(qr, wr) and np.array_equal(qc, wc)
+
+
+def test_hybrid_cross_format_directions_are_independent(oracle):
+    rng = np.random.default_rng(22)
+    bits = _bf16(rng.standard_normal((40, 24)) * 300)
+    sr, sc = np.float32(1.25), np.float32(0.03)
+    qr, qc = oracle.quantize_hybrid(bits, E4M3, sr, E5M2, sc, oracle.SRC_ORIGINAL)
+    assert np.array_equal(qr, oracle.quantize(bits, E4M3, sr)[0])
+    assert np.array_equal(qc, oracle.quantize(np.ascontiguousarray(bits.T), E5M2, sc)[0])
+
+
+def test_hybrid_rowwise_dequantized_source(oracle):
+    rng = np.random.default_rng(23)
+    bits = _bf16(rng.standard_normal((33, 50)) * 7)
+    sr = np.float32(17.0)
+    # same format and scale: re-quantizing the dequantized value gives the rowwise codes back
+    qr, qc = oracle.quantize_hybrid(bits, E4M3, sr, E4M3, sr, oracle.SRC_ROWWISE_DEQUANTIZED)
+    assert np.array_equal(qc, qr.T)
+    # the columnwise source is exactly the BF16 dequantized rowwise tensor (the documented reading)
+    sc = np.float32(0.5)
+    qr, qc = oracle.quantize_hybrid(bits, E4M3, sr, E5M2, sc, oracle.SRC_ROWWISE_DEQUANTIZED)
+    y = oracle.dequantize(qr, E4M3, np.array([np.float32(1.0) / sr]), out_dt=oracle.BF16)
+    assert np.array_equal(qc, oracle.quantize(np.ascontiguousarray(y.T), E5M2, sc)[0])
+    # E4M3 -> E5M2 from the coarser rowwise grid differs from quantizing the original
+    _, qc_orig = oracle.quantize_hybrid(bits, E4M3, sr, E5M2, sc, oracle.SRC_ORIGINAL)
+    assert not np.array_equal(qc, qc_orig)
