@@ -9,7 +9,7 @@ One step = one pass of the whole hot path over the five synthetic workloads
   W5 E5M2 current scaling + dequantize, 32 x 8192x8192
 value = algorithmic bytes (each kernel's reads once + writes once) / time, in
 GB/s, with inputs resident in HBM.  The inputs (~6.5 GB) and the step's
-traffic (~21 GB) are far larger than the 126 MB L2, so no flush is needed.
+traffic (~21 GB) are far larger than the 135 MB L2, so no flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -52,6 +52,9 @@ def parse_args():
                     help="shrink every workload's row count by this factor (testing only; 1.0 = full size)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the separately timed kernels beyond the step")
+    ap.add_argument("--extras-only", action="store_true",
+                    help="time only the separately timed kernels (MXFP8, hybrid, block cast-transpose, grouped)")
     ap.add_argument("--cpu-fraction", type=float, default=1.0 / 4,
                     help="fraction of each workload the CPU-oracle baseline processes")
     ap.add_argument("--workloads", default="W1,W2,W3,W4,W5",
@@ -360,7 +363,7 @@ def run_ours(args, rank, world):
                    "bytes": "compulsory: each workload's inputs read once + outputs written once",
                    "compulsory_bytes_per_step": step_bytes, "kernel_bytes_per_step": kernel_bytes,
                    "kernel_gbs": round(world * kernel_bytes * args.steps / (ms_max * 1e-3) / 1e9, 1),
-                   "l2": "no flush: inputs (%.2f GB) and per-step traffic (%.2f GB) exceed the 126 MB L2"
+                   "l2": "no flush: inputs (%.2f GB) and per-step traffic (%.2f GB) exceed the 135 MB L2"
                          % (sum(t.numel() * t.element_size() for t in _all_inputs(inp)) / 1e9, kernel_bytes / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
@@ -373,6 +376,8 @@ def run_ours(args, rank, world):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if full_suite and not args.no_extras:
+        result["extras"] = run_extras(inp, peak)
     if not args.no_e2e and full_suite:
         del pipes
         torch.cuda.empty_cache()
@@ -380,6 +385,102 @@ def run_ours(args, rank, world):
     if not args.no_cpu_baseline and rank == 0 and world == 1 and full_suite:
         result["cpu_baseline"] = cpu_baseline(args, inp)
     return result
+
+
+def run_extras(inp, peak, reps=10):
+    """Kernels beyond the five workloads, each timed on its own: CUDA events
+    around each call on the launching stream, an L2-sized buffer rewritten
+    before every rep (outside the events)."""
+    import torch
+    import fp8_scaled_quantization_gb300 as fq
+    dev = inp["w2"].device
+    flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for r in range(reps + 2):
+            flush.fill_(float(r))
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                tot += e0.elapsed_time(e1)
+        return tot / reps * 1e3  # us
+
+    def row(us, nbytes, what):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"what": what, "us": round(us, 2), "bytes": int(nbytes), "gbs": round(gbs, 1),
+                "frac": round(gbs / peak, 4)}
+
+    out = {}
+    x = inp["w2"]
+    r_, c_ = x.shape
+    n = x.numel()
+    qr = torch.empty((r_, c_), dtype=torch.uint8, device=dev)
+    sr = torch.empty((r_, c_ // 32), dtype=torch.uint8, device=dev)
+    qc = torch.empty((c_, r_), dtype=torch.uint8, device=dev)
+    sc = torch.empty((c_, r_ // 32), dtype=torch.uint8, device=dev)
+    us = timed(lambda: fq.fp8_quantize_mx(x, fq.E4M3, qr, sr, qc, sc))
+    out["mx_quantize_rowwise_columnwise"] = row(us, n * 2 + 2 * (n + n // 32),
+                                                "MXFP8 E4M3 1x32 + 32x1 (transposed), 8192x8192 BF16")
+    y = torch.empty((r_, c_), dtype=torch.bfloat16, device=dev)
+    us = timed(lambda: fq.fp8_dequantize_mx(qr, sr, fq.E4M3, y))
+    out["mx_dequantize"] = row(us, n + n // 32 + 2 * n, "MXFP8 E4M3 -> BF16, 8192x8192")
+    s_row = torch.full((1,), 300.0, device=dev)
+    s_col = torch.full((1,), 2.0, device=dev)
+    for src, key in ((fq.COLUMNWISE_FROM_ORIGINAL, "hybrid_from_original"),
+                     (fq.COLUMNWISE_FROM_ROWWISE_DEQUANTIZED, "hybrid_from_rowwise_dequantized")):
+        us = timed(lambda: fq.fp8_quantize_hybrid(x, fq.E4M3, s_row, qr, fq.E5M2, s_col, qc, src))
+        out[key] = row(us, n * 2 + 2 * n, "rowwise E4M3 + columnwise E5M2 (transposed), 8192x8192 BF16")
+    del qr, sr, qc, sc, y
+    a = inp["w4"][1]
+    ar, ac = a.shape
+    na = a.numel()
+    qr = torch.empty((ar, ac), dtype=torch.uint8, device=dev)
+    sr = torch.empty((ar, ac // 128), dtype=torch.float32, device=dev)
+    qc = torch.empty((ac, ar), dtype=torch.uint8, device=dev)
+    sc = torch.empty((ac, ar // 128), dtype=torch.float32, device=dev)
+    us = timed(lambda: fq.fp8_quantize_block_cast_transpose(a, fq.E4M3, qr, sr, qc, sc))
+    out["block_cast_transpose"] = row(us, na * 2 + 2 * (na + 4 * na // 128),
+                                      "E4M3 1x128 rowwise + 128x1 columnwise (transposed), 16384x7168 BF16")
+    del qr, sr, qc, sc
+    # 64 expert-sized tensors: grouped current scaling vs per-tensor calls
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    rows = torch.randint(128, 2048, (64,), generator=g, device=dev).tolist()
+    xs = [torch.randn((int(rr), 7168), generator=g, device=dev).to(torch.bfloat16) for rr in rows]
+    qs = [torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in xs]
+    m = len(xs)
+    am, s_, si_ = (torch.empty(m, device=dev) for _ in range(3))
+    nbytes = sum(t.numel() * 3 for t in xs)
+
+    def grouped():
+        fq.fp8_amax_grouped(xs, am, fq.E4M3, 0, s_, si_)
+        fq.fp8_quantize_grouped(xs, fq.E4M3, s_, qs)
+
+    def per_tensor():
+        for i, t in enumerate(xs):
+            fq.fp8_amax(t, am[i:i + 1], fq.E4M3, 0, s_[i:i + 1], si_[i:i + 1])
+            fq.fp8_quantize(t, fq.E4M3, s_[i:i + 1], qs[i])
+
+    out["grouped_current_scaling"] = row(timed(grouped), nbytes,
+                                         "64 BF16 tensors [128..2047, 7168]: amax+scale+cast, grouped (3 launches)")
+    out["per_tensor_current_scaling"] = row(timed(per_tensor), nbytes,
+                                            "the same 64 tensors, per-tensor calls (192 launches)")
+    return out
+
+
+def run_extras_only(args):
+    import torch
+    import fp8_scaled_quantization_gb300 as fq
+    fq.library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    inp = make_inputs(workload_shapes(1.0), dev, which=("W2", "W4"))
+    peak, _ = measured_hbm_peak()
+    return {"metric": METRIC, "unit": UNIT, "extras": run_extras(inp, peak, reps=max(1, args.steps))}
 
 
 def _all_inputs(inp):
@@ -600,6 +701,10 @@ def main():
         if torch.cuda.is_available():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group(backend)
+    if args.extras_only:
+        if rank == 0:
+            print(json.dumps(run_extras_only(args)), flush=True)
+        return
     res = run_ours(args, rank, world)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -19,13 +21,16 @@ from . import _lib
 E4M3, E5M2 = 0, 1
 DT_BF16, DT_FP32 = 0, 1
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
+COLUMNWISE_FROM_ORIGINAL, COLUMNWISE_FROM_ROWWISE_DEQUANTIZED = 0, 1
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 
 __all__ = [
     "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
     "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
     "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_quantize_mx", "fp8_dequantize_mx",
-    "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "launch_count", "version", "library",
+    "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "fp8_quantize_hybrid", "fp8_quantize_block_cast_transpose",
+    "fp8_amax_grouped", "fp8_quantize_grouped", "COLUMNWISE_FROM_ORIGINAL", "COLUMNWISE_FROM_ROWWISE_DEQUANTIZED",
+    "launch_count", "version", "library",
 ]
 
 
@@ -210,3 +215,60 @@ def fp8_dequantize(q, fmt, scale_inv, y, block_rows=0, block_cols=0, stream=None
         rows, cols = 1, q.numel()
     _check(library().fp8_dequantize(_p(q), fmt, rows, cols, _p(scale_inv), block_rows, block_cols, _p(y),
                                     _dt(y), _stream(stream)))
+
+
+def fp8_quantize_hybrid(x, fmt_row, scale_row, q_row, fmt_col, scale_col, q_col,
+                        source=COLUMNWISE_FROM_ORIGINAL, stream=None):
+    """Rowwise codes (fmt_row, scale_row) and transposed columnwise codes (fmt_col,
+    scale_col) from x or from the BF16-dequantized rowwise value."""
+    rows, cols = _rows_cols(x)
+    if q_row.dtype != torch.uint8 or tuple(q_row.shape) != (rows, cols):
+        raise ValueError("q_row must be uint8 [rows, cols]")
+    if q_col.dtype != torch.uint8 or tuple(q_col.shape) != (cols, rows):
+        raise ValueError("q_col must be uint8 [cols, rows]")
+    _check(library().fp8_quantize_hybrid(_p(x), _dt(x), rows, cols, fmt_row, _p(scale_row), _p(q_row), fmt_col,
+                                         _p(scale_col), _p(q_col), source, _stream(stream)))
+
+
+def fp8_quantize_block_cast_transpose(x, fmt, q_row=None, scale_inv_row=None, q_col=None, scale_inv_col=None,
+                                      stream=None):
+    """1 x 128 blockwise codes of x ([rows, cols] + fp32 [rows, ceil(cols/128)]) and of
+    x^T ([cols, rows] + fp32 [cols, ceil(rows/128)]) from one read of x."""
+    rows, cols = _rows_cols(x)
+    for t, shape, dt in ((q_row, (rows, cols), torch.uint8), (scale_inv_row, (rows, -(-cols // 128)), torch.float32),
+                         (q_col, (cols, rows), torch.uint8), (scale_inv_col, (cols, -(-rows // 128)), torch.float32)):
+        if t is not None and (t.dtype != dt or tuple(t.shape) != shape):
+            raise ValueError(f"block cast-transpose outputs must be {dt} {shape}")
+    _check(library().fp8_quantize_block_cast_transpose(_p(x), _dt(x), rows, cols, fmt, _p(q_row), _p(scale_inv_row),
+                                                       _p(q_col), _p(scale_inv_col), _stream(stream)))
+
+
+def _ptr_array(tensors):
+    return (ctypes.c_void_p * len(tensors))(*[_p(t) for t in tensors])
+
+
+def fp8_amax_grouped(xs, amax_out=None, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):
+    """Per-tensor amax (and current scale) of up to 128 tensors in one launch (+ finalize);
+    outputs are float32 device tensors of at least len(xs) elements."""
+    if not xs or len({t.dtype for t in xs}) != 1:
+        raise ValueError("xs must be a non-empty list of tensors of one dtype")
+    for out in (amax_out, scale_out, scale_inv_out):
+        if out is not None and (out.dtype != torch.float32 or out.numel() < len(xs)):
+            raise ValueError("grouped outputs must be float32 tensors of at least len(xs) elements")
+    ns = (ctypes.c_int64 * len(xs))(*[t.numel() for t in xs])
+    _check(library().fp8_amax_grouped(len(xs), _ptr_array(xs), ns, _dt(xs[0]), _p(amax_out), fmt, margin,
+                                      _p(scale_out), _p(scale_inv_out), _stream(stream)))
+
+
+def fp8_quantize_grouped(xs, fmt, scales, qs, stream=None):
+    """qs[i] = codes of xs[i] * scales[i] for up to 128 tensors in one launch."""
+    if not xs or len(xs) != len(qs) or len({t.dtype for t in xs}) != 1:
+        raise ValueError("xs and qs must be equally long lists; xs of one dtype")
+    for x, q in zip(xs, qs):
+        if q.dtype != torch.uint8 or q.numel() != x.numel():
+            raise ValueError("each q must be uint8 with as many elements as its x")
+    if scales.dtype != torch.float32 or scales.numel() < len(xs):
+        raise ValueError("scales must be a float32 tensor of at least len(xs) elements")
+    ns = (ctypes.c_int64 * len(xs))(*[t.numel() for t in xs])
+    _check(library().fp8_quantize_grouped(len(xs), _ptr_array(xs), ns, _dt(xs[0]), fmt, _p(scales), _ptr_array(qs),
+                                          _stream(stream)))

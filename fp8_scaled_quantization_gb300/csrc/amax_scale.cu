@@ -98,35 +98,88 @@ __device__ __forceinline__ float window_max(const float* hist, int len) {
 }
 
 // One CTA: reduce the partials of the previous launch and write the results.
+// Every load is issued up front (at most kFinLoads partials per thread and the
+// history entries other than this step's slot) and one block reduction
+// combines the amax maximum, the saturation sum and the window maximum of the
+// old entries; the window maximum with the new amax is then the maximum of
+// the two (NaN if either holds a NaN), which equals the maximum of the window
+// after the slot write.
+constexpr int kFinLoads = kMaxPartials / kFinThreads;
+
 template <int FMT>
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(const uint32_t* __restrict__ part_amax, const unsigned long long* __restrict__ part_sat, int nparts,
                 float* amax_out, unsigned long long* sat_out, float* scale_out, float* scale_inv_out, int margin,
                 float* hist, int hist_len, int slot, int algo) {
     pdl_begin();
-    __shared__ uint32_t red[32];
-    __shared__ unsigned long long red64[32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    uint32_t a[kFinLoads];
+    unsigned long long c[kFinLoads];
+#pragma unroll
+    for (int k = 0; k < kFinLoads; ++k) {
+        const int i = t + k * kFinThreads;
+        a[k] = (part_amax != nullptr && i < nparts) ? part_amax[i] : 0u;
+        c[k] = (part_sat != nullptr && i < nparts) ? part_sat[i] : 0ull;
+    }
+    const bool window = hist != nullptr && algo == FP8_AMAX_MAX;
+    float hm = -INFINITY;
+    int nan = 0;
+    if (window)
+        for (int i = t; i < hist_len; i += kFinThreads) {
+            if (i == slot) continue;
+            const float v = hist[i];
+            if (isnan(v)) nan = 1;
+            else hm = fmaxf(hm, v);
+        }
     uint32_t bits = 0;
     unsigned long long sat = 0;
-    for (int i = threadIdx.x; i < nparts; i += kFinThreads) {
-        if (part_amax) bits = umax(bits, part_amax[i]);
-        if (part_sat) sat += part_sat[i];
+#pragma unroll
+    for (int k = 0; k < kFinLoads; ++k) {
+        bits = umax(bits, a[k]);
+        sat += c[k];
     }
-    bits = block_max_u32(bits, red);
-    if (part_sat) sat = block_sum_u64(sat, red64);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, o));
+        sat += __shfl_xor_sync(0xFFFFFFFFu, sat, o);
+        hm = fmaxf(hm, __shfl_xor_sync(0xFFFFFFFFu, hm, o));
+        nan |= __shfl_xor_sync(0xFFFFFFFFu, nan, o);
+    }
+    __shared__ uint32_t s_bits[32];
+    __shared__ unsigned long long s_sat[32];
+    __shared__ float s_hm[32];
+    __shared__ int s_nan[32];
+    if (lane == 0) {
+        s_bits[warp] = bits;
+        s_sat[warp] = sat;
+        s_hm[warp] = hm;
+        s_nan[warp] = nan;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    constexpr int kWarps = kFinThreads / 32;
+    bits = lane < kWarps ? s_bits[lane] : 0u;
+    sat = lane < kWarps ? s_sat[lane] : 0ull;
+    hm = lane < kWarps ? s_hm[lane] : -INFINITY;
+    nan = lane < kWarps ? s_nan[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, o));
+        sat += __shfl_xor_sync(0xFFFFFFFFu, sat, o);
+        hm = fmaxf(hm, __shfl_xor_sync(0xFFFFFFFFu, hm, o));
+        nan |= __shfl_xor_sync(0xFFFFFFFFu, nan, o);
+    }
+    if (lane != 0) return;
     if (bits > 0x7F800000u) bits = 0x7FC00000u;  // canonical NaN
     const float amax = __uint_as_float(bits);
-    if (threadIdx.x == 0) {
-        if (amax_out) *amax_out = amax;
-        if (sat_out) *sat_out = sat;
-    }
+    if (amax_out) *amax_out = amax;
+    if (sat_out) *sat_out = sat;
     float eff = amax;
     if (hist != nullptr) {
-        if (threadIdx.x == 0) hist[slot] = amax;
-        __syncthreads();  // the slot write is visible to the whole CTA
-        if (algo == FP8_AMAX_MAX) eff = window_max(hist, hist_len);
+        hist[slot] = amax;
+        if (window) eff = (nan || isnan(amax)) ? __uint_as_float(0x7FC00000u) : fmaxf(hm, amax);
     }
-    if (threadIdx.x == 0 && scale_out != nullptr) {
+    if (scale_out != nullptr) {
         float s, si;
         scale_from_amax<FMT>(eff, margin, &s, &si);
         *scale_out = s;

@@ -43,14 +43,45 @@ __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t 
     b3 = __byte_perm(t1, t3, 0x7632);
 }
 
-template <int FMT, bool BF16, bool AMAX>
+// Where the columnwise codes come from ("[Pytorch][Common] Hybrid quantization
+// #2817", columnwise_source): kSame -- the rowwise codes themselves (one format
+// and scale); kOriginal -- x, in the columnwise format and scale;
+// kRowDequant -- the BF16 dequantized rowwise value.
+constexpr int kSame = 0, kOriginal = 1, kRowDequant = 2;
+
+// 8 rowwise codes -> 8 BF16 values: RNE_bf16(fl32(decode(code) * scale_inv)).
+template <int FMT>
+__device__ __forceinline__ uint4 dequant8_bf16(uint32_t lo, uint32_t hi, float si) {
+    const uint32_t w[2] = {lo, hi};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t h01 = fp8x2_to_f16x2<FMT>(w[i] & 0xFFFFu), h23 = fp8x2_to_f16x2<FMT>(w[i] >> 16);
+        out[2 * i] = f32x2_to_bf16x2(__fmul_rn(f16_lo_to_f32(h01), si), __fmul_rn(f16_hi_to_f32(h01), si));
+        out[2 * i + 1] = f32x2_to_bf16x2(__fmul_rn(f16_lo_to_f32(h23), si), __fmul_rn(f16_hi_to_f32(h23), si));
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Columnwise codes of 8 BF16 values (with the exact slow path for Inf / NaN).
+template <int FMT_COL>
+__device__ __forceinline__ Codes8 col_codes_bf16x8(uint4 v, float scale) {
+    uint32_t m;
+    Codes8 c = cvt_bf16x8<FMT_COL>(v, scale, &m);
+    if (chunk_needs_fixup<FMT_COL, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT_COL>(v, scale, &c);
+    return c;
+}
+
+template <int FMT, bool BF16, bool AMAX, int FMT_COL = FMT, int SRC = kSame>
 __global__ void __launch_bounds__(kThreads)
 cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ scale_ptr,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ q_col, int vec_ok,
-                      uint32_t* __restrict__ part_amax) {
+                      uint32_t* __restrict__ part_amax, const float* __restrict__ scale_col_ptr) {
     pdl_begin();
     __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
     const float scale = __ldg(scale_ptr);
+    const float scale_col = SRC == kSame ? scale : __ldg(scale_col_ptr);
+    const float scale_inv_row = SRC == kRowDequant ? __fdiv_rn(1.0f, scale) : 1.0f;
     // Tiles run in reverse order with evict_first loads: after an amax pass over
     // x (current scaling) the end of x is the part still in L2.
     const int64_t r0 = (int64_t)(gridDim.y - 1 - blockIdx.y) * kTile, c0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * kTile;
@@ -76,7 +107,11 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
                 if constexpr (AMAX) m16 = max_u16x2(m16, m);
                 const int r = p * 16 + rsub;
                 if (q_row) stg_stream(q_row + (r0 + r) * cols + c0 + cc * 8, make_uint2(c.lo, c.hi));
-                *reinterpret_cast<uint2*>(&tile[r * 32 + ((cc * 2) ^ (p << 2))]) = make_uint2(c.lo, c.hi);
+                Codes8 cc8 = c;
+                if constexpr (SRC == kOriginal) cc8 = col_codes_bf16x8<FMT_COL>(v[p], scale_col);
+                if constexpr (SRC == kRowDequant)
+                    cc8 = col_codes_bf16x8<FMT_COL>(dequant8_bf16<FMT>(c.lo, c.hi, scale_inv_row), scale_col);
+                *reinterpret_cast<uint2*>(&tile[r * 32 + ((cc * 2) ^ (p << 2))]) = make_uint2(cc8.lo, cc8.hi);
             }
             if constexpr (AMAX) am = fold_u16x2_to_f32bits(m16);
         } else {
@@ -98,7 +133,20 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
                     if constexpr (AMAX) am = umax(am, m);
                     const int r = (half * 8 + p) * 8 + rsub;
                     if (q_row) *reinterpret_cast<uint32_t*>(q_row + (r0 + r) * cols + c0 + lane * 4) = w;
-                    tile[r * 32 + (lane ^ swz(r))] = w;
+                    uint32_t wc = w;
+                    if constexpr (SRC == kOriginal) {
+                        uint32_t m2;
+                        wc = cvt_f32x4<FMT_COL>(f, scale_col, &m2);
+                        if (chunk_needs_fixup<FMT_COL, false>(m2, scale_col)) fixup_f32x4<FMT_COL>(f, scale_col, &wc);
+                    }
+                    if constexpr (SRC == kRowDequant) {
+                        const uint4 d = dequant8_bf16<FMT>(w, 0u, scale_inv_row);  // 4 values in d.x, d.y
+                        const float4 g = make_float4(bf16lo(d.x), bf16hi(d.x), bf16lo(d.y), bf16hi(d.y));
+                        uint32_t m2;
+                        wc = cvt_f32x4<FMT_COL>(g, scale_col, &m2);
+                        if (chunk_needs_fixup<FMT_COL, false>(m2, scale_col)) fixup_f32x4<FMT_COL>(g, scale_col, &wc);
+                    }
+                    tile[r * 32 + (lane ^ swz(r))] = wc;
                 }
             }
         }
@@ -144,7 +192,13 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
                 const uint8_t code = (uint8_t)quant_one<FMT>(xv, scale, &s);
                 am = umax(am, b);
                 if (q_row) q_row[e] = code;
-                tb[r * kTile + c] = code;
+                uint8_t ccode = code;
+                if constexpr (SRC == kOriginal) ccode = (uint8_t)quant_one<FMT_COL>(xv, scale_col, &s);
+                if constexpr (SRC == kRowDequant) {
+                    const uint4 d = dequant8_bf16<FMT>(code, 0u, scale_inv_row);
+                    ccode = (uint8_t)quant_one<FMT_COL>(bf16lo(d.x), scale_col, &s);
+                }
+                tb[r * kTile + c] = ccode;
             }
         }
         __syncthreads();
@@ -169,9 +223,9 @@ fp8_status_t launch_ct(bool amax, dim3 grid, cudaStream_t st, const uint8_t* x, 
     const char* w = "fp8_quantize_cast_transpose";
     if (amax)
         return launch(w, cast_transpose_kernel<FMT, BF16, true>, grid, dim3(kThreads), st, x, rows, cols, scale, q_row,
-                      q_col, vec_ok, pa);
+                      q_col, vec_ok, pa, static_cast<const float*>(nullptr));
     return launch(w, cast_transpose_kernel<FMT, BF16, false>, grid, dim3(kThreads), st, x, rows, cols, scale, q_row,
-                  q_col, vec_ok, pa);
+                  q_col, vec_ok, pa, static_cast<const float*>(nullptr));
 }
 
 }  // namespace
@@ -229,4 +283,41 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
     fa.amax_out = amax_out;
     fa.fmt = (int)fmt;
     return launch_finalize(fa, st);
+}
+
+extern "C" fp8_status_t fp8_quantize_hybrid(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
+                                            fp8_format_t fmt_row, const float* scale_row, uint8_t* q_row,
+                                            fp8_format_t fmt_col, const float* scale_col, uint8_t* q_col,
+                                            fp8_columnwise_source_t source, void* stream) {
+    const char* fn = "fp8_quantize_hybrid";
+    if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!valid_fmt(fmt_row) || !valid_fmt(fmt_col)) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", fn);
+    if (source != FP8_COLUMNWISE_FROM_ORIGINAL && source != FP8_COLUMNWISE_FROM_ROWWISE_DEQUANTIZED)
+        return fail(FP8_ERR_INVALID_ARG, "%s: unknown columnwise source %d", fn, (int)source);
+    if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
+    if (scale_row == nullptr || scale_col == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: scale is NULL", fn);
+    const int64_t n = rows * cols;
+    if (n == 0) return FP8_OK;
+    if (x == nullptr || q_row == nullptr || q_col == nullptr)
+        return fail(FP8_ERR_INVALID_ARG, "%s: x / q_row / q_col is NULL", fn);
+    if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
+    const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;
+    if (gy > 65535 || gx > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "%s: shape too large", fn);
+    const int vec_ok = aligned16(x) && aligned16(q_row) && aligned16(q_col) && cols % 16 == 0 && rows % 16 == 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t* xp = static_cast<const uint8_t*>(x);
+    const dim3 grid((unsigned)gx, (unsigned)gy), block(kThreads);
+    uint32_t* none = nullptr;
+    const bool deq = source == FP8_COLUMNWISE_FROM_ROWWISE_DEQUANTIZED;
+#define FP8Q_HYB(FR, FC, B)                                                                                           \
+    (deq ? launch(fn, cast_transpose_kernel<FR, B, false, FC, kRowDequant>, grid, block, st, xp, rows, cols, scale_row, \
+                  q_row, q_col, vec_ok, none, scale_col)                                                              \
+         : launch(fn, cast_transpose_kernel<FR, B, false, FC, kOriginal>, grid, block, st, xp, rows, cols, scale_row,   \
+                  q_row, q_col, vec_ok, none, scale_col))
+    const bool bf16 = dtype == FP8_DT_BF16;
+    if (fmt_row == FP8_E4M3 && fmt_col == FP8_E4M3) return bf16 ? FP8Q_HYB(kE4M3, kE4M3, true) : FP8Q_HYB(kE4M3, kE4M3, false);
+    if (fmt_row == FP8_E4M3) return bf16 ? FP8Q_HYB(kE4M3, kE5M2, true) : FP8Q_HYB(kE4M3, kE5M2, false);
+    if (fmt_col == FP8_E4M3) return bf16 ? FP8Q_HYB(kE5M2, kE4M3, true) : FP8Q_HYB(kE5M2, kE4M3, false);
+    return bf16 ? FP8Q_HYB(kE5M2, kE5M2, true) : FP8Q_HYB(kE5M2, kE5M2, false);
+#undef FP8Q_HYB
 }

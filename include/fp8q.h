@@ -84,6 +84,12 @@ typedef enum { FP8_DT_BF16 = 0, FP8_DT_FP32 = 1 } fp8_dtype_t;
 /* "Megatron FP8" §5 / §7: amax_compute_algo of the delayed recipe. */
 typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
 
+/* "[Pytorch][Common] Hybrid quantization #2817", columnwise_source. */
+typedef enum {
+    FP8_COLUMNWISE_FROM_ORIGINAL = 0,            /* quantize x itself                            */
+    FP8_COLUMNWISE_FROM_ROWWISE_DEQUANTIZED = 1  /* quantize the BF16 dequantized rowwise value */
+} fp8_columnwise_source_t;
+
 typedef enum {
     FP8_OK = 0,
     FP8_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad enum or margin */
@@ -229,6 +235,28 @@ fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64
                                          void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Hybrid per-direction quantization                                         */
+/* ------------------------------------------------------------------------ */
+/* "[Pytorch][Common] Hybrid quantization #2817": the rowwise and columnwise
+ * copies may use different per-tensor formats and scales, and the columnwise
+ * copy may be quantized from the original tensor or from the dequantized
+ * rowwise value (columnwise_source).  One read of x gives
+ *   q_row [rows, cols] = codes of x in fmt_row with *scale_row,
+ *   q_col [cols, rows] = codes, in fmt_col with *scale_col, of
+ *     x^T                                       (FROM_ORIGINAL), or
+ *     RNE_bf16(fl32(decode(q_row) * fl32(1 / *scale_row)))^T
+ *                                               (FROM_ROWWISE_DEQUANTIZED:
+ *                                                the value fp8_dequantize
+ *                                                would produce).
+ * With one format and one scale and FROM_ORIGINAL this is
+ * fp8_quantize_cast_transpose.  Both outputs are required; same layouts and
+ * alignment rules as fp8_quantize_cast_transpose.  One kernel launch. */
+fp8_status_t fp8_quantize_hybrid(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
+                                 fp8_format_t fmt_row, const float* scale_row, uint8_t* q_row,
+                                 fp8_format_t fmt_col, const float* scale_col, uint8_t* q_col,
+                                 fp8_columnwise_source_t source, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Block-scaled quantize (128x128 and 1x128)                                 */
 /* ------------------------------------------------------------------------ */
 /* "Low Precision Training and Rollout": block FP8 with 128x128 blocks
@@ -250,6 +278,44 @@ fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64
 fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
                                 int block_rows, int block_cols, fp8_format_t fmt, uint8_t* q_out,
                                 float* scale_inv_out, void* stream);
+
+/* Blockwise cast + transpose: "[Pytorch][Common] Hybrid quantization #2817"
+ * (Float8Blockwise sub-storage with a columnwise copy for the backward GEMM,
+ * columnwise_source = original).  One read of x gives
+ *   q_row [rows, cols] + scale_inv_row [rows, ceil(cols/128)]: the 1 x 128
+ *       blockwise quantization of x (as fp8_quantize_block(1, 128));
+ *   q_col [cols, rows] + scale_inv_col [cols, ceil(rows/128)]: the 1 x 128
+ *       blockwise quantization of x^T, i.e. 128 x 1 blocks along the columns
+ *       of x, written transposed.
+ * Either direction may be NULL (codes and scales together).  BF16 inputs with
+ * rows and cols multiples of 128 and 16-byte aligned x / codes use one kernel
+ * over 128 x 128 tiles; other shapes use one guarded kernel per direction. */
+fp8_status_t fp8_quantize_block_cast_transpose(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
+                                               fp8_format_t fmt, uint8_t* q_row, float* scale_inv_row,
+                                               uint8_t* q_col, float* scale_inv_col, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped (multi-tensor) current scaling                                    */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §21: every expert of an MoE layer keeps its own per-tensor
+ * FP8 scaling state; §24: the amax / scale overhead should stay a small share
+ * of the step.  These two calls treat up to 128 tensors as one launch each
+ * (plus one finalize), instead of two or three launches per tensor.
+ *
+ * fp8_amax_grouped: amax_out[i] = max |xs[i]| and, when scale_out /
+ *   scale_inv_out are given, the current scale of tensor i by the scale rule
+ *   with `margin`.  Outputs are device float arrays of `count` entries.
+ * fp8_quantize_grouped: qs[i] = codes of xs[i] * scales[i] (scales: device
+ *   float[count]).
+ *   count      1 .. 128; xs, ns, qs are HOST arrays of `count` entries
+ *              holding device pointers / element counts.
+ *   xs[i], qs[i] must be 16-byte aligned when ns[i] > 0 (else
+ *              FP8_ERR_UNSUPPORTED); all tensors share `dtype`. */
+fp8_status_t fp8_amax_grouped(int count, const void* const* xs, const int64_t* ns, fp8_dtype_t dtype,
+                              float* amax_out, fp8_format_t fmt, int margin, float* scale_out,
+                              float* scale_inv_out, void* stream);
+fp8_status_t fp8_quantize_grouped(int count, const void* const* xs, const int64_t* ns, fp8_dtype_t dtype,
+                                  fp8_format_t fmt, const float* scales, uint8_t* const* qs, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Dequantize                                                                */

@@ -71,12 +71,15 @@ def test_mx_single_direction(cuda, oracle):
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
-def test_mx_dequantize_matches_oracle(cuda, oracle, out_dtype, fmt):
-    g = torch.Generator(device="cpu").manual_seed(3)
-    q = torch.randint(0, 256, (37, 100), generator=g, dtype=torch.uint8)
-    s = torch.randint(0, 256, (37, 4), generator=g, dtype=torch.uint8)
-    s[0, :] = torch.tensor([0, 1, 254, 255], dtype=torch.uint8)
-    y = torch.empty((37, 100), dtype=out_dtype, device=cuda)
+@pytest.mark.parametrize("shape", [(37, 100), (64, 256), (3, 4096), (1, 32)])
+def test_mx_dequantize_matches_oracle(cuda, oracle, out_dtype, fmt, shape):
+    # (37, 100): the general kernel; the others have cols % 32 == 0 (vector kernel)
+    rows, cols = shape
+    g = torch.Generator(device="cpu").manual_seed(3 + rows)
+    q = torch.randint(0, 256, shape, generator=g, dtype=torch.uint8)
+    s = torch.randint(0, 256, (rows, -(-cols // 32)), generator=g, dtype=torch.uint8)
+    s.view(-1)[:4] = torch.tensor([0, 1, 254, 255], dtype=torch.uint8)[: s.numel()]
+    y = torch.empty(shape, dtype=out_dtype, device=cuda)
     fq.fp8_dequantize_mx(q.to(cuda), s.to(cuda), fmt, y)
     torch.cuda.synchronize()
     want = oracle.dequantize_mx(q.numpy(), s.numpy(), fmt, out_dt=oracle.BF16 if out_dtype == torch.bfloat16 else oracle.FP32)

@@ -440,3 +440,127 @@ def test_errors_are_raised(cuda):
     with pytest.raises(fq.Fp8Error):
         fq.fp8_update_scale_delayed(torch.zeros(0, device=cuda), 0, None, fq.AMAX_MAX, E4M3, 0,
                                     torch.empty(1, device=cuda), torch.empty(1, device=cuda))
+
+
+# ---------------------------------------------------------------------------
+# Blockwise cast + transpose (1 x 128 rowwise, 128 x 1 columnwise)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (130, 200), (1, 300), (384, 1)])
+def test_block_cast_transpose_matches_oracle(cuda, oracle, dtype, fmt, shape):
+    rows, cols = shape
+    g = torch.Generator(device="cpu").manual_seed(rows * 7 + cols)
+    x = (torch.randn(shape, generator=g) * torch.exp(2 * torch.randn((rows, 1), generator=g))
+         * torch.exp(2 * torch.randn((1, cols), generator=g))).to(dtype).to(cuda)
+    if x.numel() > 500:
+        x = with_specials(x, 3)
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+    s_row = torch.empty((rows, -(-cols // 128)), dtype=torch.float32, device=cuda)
+    q_col = torch.empty((cols, rows), dtype=torch.uint8, device=cuda)
+    s_col = torch.empty((cols, -(-rows // 128)), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block_cast_transpose(x, fmt, q_row, s_row, q_col, s_col)
+    torch.cuda.synchronize()
+    xb = host_bits(x)
+    wq, ws = oracle.quantize_block(xb, 1, 128, fmt)
+    assert np.array_equal(s_row.cpu().numpy().view(np.uint32), ws.view(np.uint32))
+    assert np.array_equal(q_row.cpu().numpy(), wq)
+    wqt, wst = oracle.quantize_block(np.ascontiguousarray(xb.T), 1, 128, fmt)
+    assert np.array_equal(s_col.cpu().numpy().view(np.uint32), wst.view(np.uint32))
+    assert np.array_equal(q_col.cpu().numpy(), wqt)
+
+
+def test_block_cast_transpose_tile_without_specials(cuda, oracle):
+    """A 512 x 512 BF16 tensor with no Inf / NaN: every tile takes the paired
+    two-value conversion of the columnwise codes."""
+    g = torch.Generator(device="cpu").manual_seed(77)
+    x = (torch.randn((512, 512), generator=g) * torch.exp(3 * torch.randn((1, 512), generator=g))).to(torch.bfloat16)
+    x = x.to(cuda)
+    q = torch.empty((512, 512), dtype=torch.uint8, device=cuda)
+    s = torch.empty((512, 4), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block_cast_transpose(x, E5M2, None, None, q, s)
+    torch.cuda.synchronize()
+    wq, ws = oracle.quantize_block(np.ascontiguousarray(host_bits(x).T), 1, 128, E5M2)
+    assert np.array_equal(q.cpu().numpy(), wq) and np.array_equal(s.cpu().numpy(), ws)
+
+
+def test_block_cast_transpose_one_direction(cuda, oracle):
+    x = random_input((256, 512), torch.bfloat16, 17, cuda)
+    q = torch.empty((512, 256), dtype=torch.uint8, device=cuda)
+    s = torch.empty((512, 2), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block_cast_transpose(x, E4M3, None, None, q, s)
+    torch.cuda.synchronize()
+    wq, ws = oracle.quantize_block(np.ascontiguousarray(host_bits(x).T), 1, 128, E4M3)
+    assert np.array_equal(q.cpu().numpy(), wq) and np.array_equal(s.cpu().numpy(), ws)
+    q2 = torch.empty((256, 512), dtype=torch.uint8, device=cuda)
+    s2 = torch.empty((256, 4), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block_cast_transpose(x, E4M3, q2, s2)
+    torch.cuda.synchronize()
+    wq2, ws2 = oracle.quantize_block(host_bits(x), 1, 128, E4M3)
+    assert np.array_equal(q2.cpu().numpy(), wq2) and np.array_equal(s2.cpu().numpy(), ws2)
+
+
+# ---------------------------------------------------------------------------
+# Hybrid per-direction quantization ("[Pytorch][Common] Hybrid quantization #2817")
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("fmts", [(E4M3, E5M2), (E5M2, E4M3), (E4M3, E4M3), (E5M2, E5M2)])
+@pytest.mark.parametrize("source", [fq.COLUMNWISE_FROM_ORIGINAL, fq.COLUMNWISE_FROM_ROWWISE_DEQUANTIZED])
+@pytest.mark.parametrize("shape", [(256, 384), (130, 200), (48, 16), (1, 1)])
+def test_hybrid_matches_oracle(cuda, oracle, dtype, fmts, source, shape):
+    fmt_row, fmt_col = fmts
+    rows, cols = shape
+    x = random_input(shape, dtype, rows * 31 + cols + source, cuda)
+    if x.numel() > 500:
+        x = with_specials(x, 5)
+    # Scales that put part of the tensor past each format's maximum, so that both
+    # the fast path and the saturating slow path run.
+    s_row, s_col = np.float32(3.0e2), np.float32(0.37)
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((cols, rows), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_hybrid(x, fmt_row, dev_scalar(s_row, cuda), q_row, fmt_col, dev_scalar(s_col, cuda), q_col,
+                           source)
+    torch.cuda.synchronize()
+    wr, wc = oracle.quantize_hybrid(host_bits(x), fmt_row, s_row, fmt_col, s_col, source)
+    assert np.array_equal(q_row.cpu().numpy(), wr)
+    assert np.array_equal(q_col.cpu().numpy(), wc)
+
+
+def test_hybrid_same_format_and_scale_is_cast_transpose(cuda):
+    x = random_input((384, 512), torch.bfloat16, 41, cuda)
+    s = dev_scalar(np.float32(17.0), cuda)
+    q_row = torch.empty((384, 512), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((512, 384), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_hybrid(x, E4M3, s, q_row, E4M3, s, q_col, fq.COLUMNWISE_FROM_ORIGINAL)
+    r2 = torch.empty_like(q_row)
+    c2 = torch.empty_like(q_col)
+    fq.fp8_quantize_cast_transpose(x, E4M3, s, r2, c2)
+    torch.cuda.synchronize()
+    assert torch.equal(q_row, r2) and torch.equal(q_col, c2)
+
+
+def test_hybrid_dequantized_source_matches_dequantize_then_quantize(cuda):
+    """Columnwise-from-dequantized equals: dequantize the rowwise codes to BF16 with
+    fp8_dequantize, then cast-transpose that tensor in the columnwise format."""
+    x = random_input((256, 256), torch.bfloat16, 43, cuda)
+    s_row, s_col = dev_scalar(np.float32(64.0), cuda), dev_scalar(np.float32(2.5), cuda)
+    q_row = torch.empty((256, 256), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((256, 256), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_hybrid(x, E4M3, s_row, q_row, E5M2, s_col, q_col, fq.COLUMNWISE_FROM_ROWWISE_DEQUANTIZED)
+    si = dev_scalar(np.float32(1.0 / 64.0), cuda)
+    y = torch.empty((256, 256), dtype=torch.bfloat16, device=cuda)
+    fq.fp8_dequantize(q_row, E4M3, si, y)
+    q2 = torch.empty_like(q_col)
+    fq.fp8_quantize_cast_transpose(y, E5M2, s_col, None, q2)
+    torch.cuda.synchronize()
+    assert torch.equal(q_col, q2)
+
+
+def test_hybrid_rejects_bad_source(cuda):
+    x = torch.zeros((16, 16), dtype=torch.bfloat16, device=cuda)
+    s = dev_scalar(np.float32(1.0), cuda)
+    q = torch.empty((16, 16), dtype=torch.uint8, device=cuda)
+    with pytest.raises(fq.Fp8Error):
+        fq.fp8_quantize_hybrid(x, E4M3, s, q, E5M2, s, q.clone(), 7)

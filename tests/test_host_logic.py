@@ -70,6 +70,21 @@ BAD = 0x1000  # never dereferenced: every call below is rejected on the host fir
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 32, 32, BAD, 0, None), 2, "block shape"),
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 0, 0, BAD, 7, None), 1, "out_dtype"),
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD + 2, 0, 0, BAD, 0, None), 1, "scale_inv not 4-byte"),
+    (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, BAD, BAD, 1, BAD, BAD, 5, None), 1, "columnwise source"),
+    (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, BAD, BAD, 3, BAD, BAD, 0, None), 1, "unknown format"),
+    (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, None, BAD, 1, BAD, BAD, 0, None), 1, "scale is NULL"),
+    (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, BAD, None, 1, BAD, BAD, 1, None), 1, "q_col is NULL"),
+    (lambda L: L.fp8_quantize_block_cast_transpose(BAD, 0, 4, 4, 0, BAD, None, None, None, None), 1,
+     "both its codes and its scales"),
+    (lambda L: L.fp8_quantize_block_cast_transpose(BAD, 0, 4, 4, 0, None, None, None, None, None), 1,
+     "no output requested"),
+    (lambda L: L.fp8_quantize_block_cast_transpose(BAD, 0, 4, 4, 0, BAD, BAD + 2, None, None, None), 1,
+     "not 4-byte aligned"),
+    (lambda L: L.fp8_amax_grouped(0, BAD, BAD, 0, BAD, 0, 0, None, None, None), 1, "count must be"),
+    (lambda L: L.fp8_amax_grouped(129, BAD, BAD, 0, BAD, 0, 0, None, None, None), 1, "count must be"),
+    (lambda L: L.fp8_amax_grouped(2, BAD, BAD, 0, None, 0, 0, None, None, None), 1, "no output requested"),
+    (lambda L: L.fp8_quantize_grouped(2, None, BAD, 0, 0, BAD, BAD, None), 1, "is NULL"),
+    (lambda L: L.fp8_quantize_grouped(2, BAD, BAD, 0, 0, None, BAD, None), 1, "scales is NULL"),
 ])
 def test_host_validation_rejects_before_launch(native_lib, call, status, msg):
     before = native_lib.fp8_launch_count()
@@ -175,3 +190,17 @@ def test_reference_arm_nonzero_rank_exits_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"], env=env,
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_grouped_binding_marshals_and_rejects_host_tensors():
+    """The grouped bindings build their host pointer / size tables before the
+    device check rejects CPU tensors (no CUDA call is made)."""
+    import fp8_scaled_quantization_gb300 as fq
+    xs = [torch.zeros(16, dtype=torch.bfloat16), torch.zeros(32, dtype=torch.bfloat16)]
+    with pytest.raises(ValueError, match="CUDA device"):
+        fq.fp8_amax_grouped(xs, torch.zeros(2))
+    with pytest.raises(ValueError, match="CUDA device"):
+        fq.fp8_quantize_grouped(xs, fq.E4M3, torch.zeros(2), [torch.zeros(16, dtype=torch.uint8),
+                                                               torch.zeros(32, dtype=torch.uint8)])
+    with pytest.raises(ValueError, match="at least len"):
+        fq.fp8_amax_grouped(xs, torch.zeros(1))
