@@ -185,8 +185,8 @@ mx_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, 
 }
 
 // Fast MX dequantize: cols % 32 == 0 and 16-byte aligned q / y, so the block of
-// flat element e is e / 32; each thread converts 16-code units, 8 loads in
-// flight, one scale byte per unit.
+// flat element e is e / 32; each thread converts 16-code units, 8 in flight,
+// loading each unit's scale byte together with its codes.
 template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 mx_dequant_vec_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t n,
@@ -196,32 +196,44 @@ mx_dequant_vec_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
     const int64_t nunits = n / 16;
     const int64_t ub = (int64_t)blockIdx.x * kThreads * kU + threadIdx.x;
     uint4 c[kU];
+    uint32_t code[kU];
 #pragma unroll
     for (int k = 0; k < kU; ++k) {
         const int64_t u = ub + (int64_t)k * kThreads;
-        if (u < nunits) c[k] = ldg_stream(q + u * 16);
+        if (u < nunits) {
+            c[k] = ldg_stream(q + u * 16);
+            code[k] = s[u >> 1];  // 16-code unit u lies in 32-element block u / 2
+        }
     }
 #pragma unroll
     for (int k = 0; k < kU; ++k) {
         const int64_t u = ub + (int64_t)k * kThreads;
         if (u >= nunits) continue;
-        const uint32_t code = __ldg(s + (u >> 1));  // 16-code unit u lies in 32-element block u / 2
-        const float m = code == 0xFFu ? __uint_as_float(0x7FFFFFFFu)
-                                      : (code == 0u ? __uint_as_float(0x00400000u) : exp2i((int)code - 127));
+        const float m = code[k] == 0xFFu ? __uint_as_float(0x7FFFFFFFu)
+                                         : (code[k] == 0u ? __uint_as_float(0x00400000u) : exp2i((int)code[k] - 127));
         const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+        float f[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t h01 = fp8x2_to_f16x2<FMT>(w[i] & 0xFFFFu), h23 = fp8x2_to_f16x2<FMT>(w[i] >> 16);
-            const float f0 = __fmul_rn(f16_lo_to_f32(h01), m), f1 = __fmul_rn(f16_hi_to_f32(h01), m);
-            const float f2 = __fmul_rn(f16_lo_to_f32(h23), m), f3 = __fmul_rn(f16_hi_to_f32(h23), m);
-            if constexpr (OUT_BF16) {
-                __stcs(reinterpret_cast<uint2*>(y + u * 32 + i * 8),
-                       make_uint2(f32x2_to_bf16x2(f0, f1), f32x2_to_bf16x2(f2, f3)));
-            } else {
-                const float f[4] = {f0, f1, f2, f3};
+            f[4 * i + 0] = __fmul_rn(f16_lo_to_f32(h01), m);
+            f[4 * i + 1] = __fmul_rn(f16_hi_to_f32(h01), m);
+            f[4 * i + 2] = __fmul_rn(f16_lo_to_f32(h23), m);
+            f[4 * i + 3] = __fmul_rn(f16_hi_to_f32(h23), m);
+        }
+        if constexpr (OUT_BF16) {
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = f32x2_to_bf16x2(f[2 * i], f[2 * i + 1]);
+            stg_stream(y + u * 32, make_uint4(o[0], o[1], o[2], o[3]));
+            stg_stream(y + u * 32 + 16, make_uint4(o[4], o[5], o[6], o[7]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
                 uint32_t o[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = isnan(f[j]) ? 0x7FFFFFFFu : __float_as_uint(f[j]);
+                for (int j = 0; j < 4; ++j)
+                    o[j] = isnan(f[4 * i + j]) ? 0x7FFFFFFFu : __float_as_uint(f[4 * i + j]);
                 stg_stream(y + (u * 16 + 4 * i) * 4, make_uint4(o[0], o[1], o[2], o[3]));
             }
         }
