@@ -564,3 +564,30 @@ def test_hybrid_rejects_bad_source(cuda):
     q = torch.empty((16, 16), dtype=torch.uint8, device=cuda)
     with pytest.raises(fq.Fp8Error):
         fq.fp8_quantize_hybrid(x, E4M3, s, q, E5M2, s, q.clone(), 7)
+
+
+# ---------------------------------------------------------------------------
+# Back-to-back reductions on one stream
+# ---------------------------------------------------------------------------
+
+def test_back_to_back_reductions_do_not_mix(cuda, oracle):
+    """A large amax / count followed by a small one on the same stream (and the
+    same workspace) must report the small one."""
+    big = random_input(3_000_000, torch.bfloat16, 61, cuda) * 1000
+    small = random_input(5000, torch.bfloat16, 62, cuda)
+    am, s, si = (torch.empty(1, device=cuda) for _ in range(3))
+    sat = torch.empty(1, dtype=torch.int64, device=cuda)
+    q_big = torch.empty(big.shape, dtype=torch.uint8, device=cuda)
+    q_small = torch.empty(small.shape, dtype=torch.uint8, device=cuda)
+    one = dev_scalar(np.float32(1.0), cuda)
+    for _ in range(2):
+        fq.fp8_amax(big, am)
+        fq.fp8_amax(small, am, E4M3, 0, s, si)
+        torch.cuda.synchronize()
+        assert f32_bits(am.item()) == f32_bits(oracle.amax(host_bits(small)))
+        fq.fp8_quantize(big, E4M3, one, q_big, am, sat)
+        fq.fp8_quantize(small, E4M3, one, q_small, am, sat)
+        torch.cuda.synchronize()
+        _, wsat = oracle.quantize(host_bits(small), E4M3, np.float32(1.0))
+        assert sat.item() == wsat and f32_bits(am.item()) == f32_bits(oracle.amax(host_bits(small)))
+
