@@ -28,10 +28,11 @@ template <bool BF16> struct VecCfg {
     static constexpr int64_t kUnitsPerCta = (int64_t)kThreads * kUnits;
 };
 
-// At most 48 registers, so that 5 CTAs (1280 threads, 160 KB of loads in
-// flight) fit on an SM whichever reductions are fused in.
+// The plain cast fits 48 registers, so 5 CTAs (1280 threads, 160 KB of loads
+// in flight) share an SM; the reducing variants need more (at 48 they spill
+// inside the loop) and take 64 registers, 4 CTAs per SM.
 template <int FMT, bool BF16, bool AMAX, bool SAT>
-__global__ void __launch_bounds__(kThreads, 5)
+__global__ void __launch_bounds__(kThreads, (AMAX || SAT) ? 4 : 5)
 quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int64_t n, const float* scale_ptr,
                     uint32_t* __restrict__ part_amax, unsigned long long* __restrict__ part_sat) {
     pdl_begin();
