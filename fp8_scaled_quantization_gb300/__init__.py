@@ -28,7 +28,7 @@ __all__ = [
     "E4M3", "E5M2", "DT_BF16", "DT_FP32", "AMAX_MAX", "AMAX_MOST_RECENT", "FP8_MAX", "Fp8Error",
     "fp8_amax", "fp8_update_scale_delayed", "fp8_quantize", "fp8_quantize_cast_transpose",
     "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_quantize_mx", "fp8_dequantize_mx",
-    "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "fp8_quantize_hybrid", "fp8_quantize_block_cast_transpose",
+    "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "fp8_quantize_current", "fp8_quantize_hybrid", "fp8_quantize_block_cast_transpose",
     "fp8_amax_grouped", "fp8_quantize_grouped", "COLUMNWISE_FROM_ORIGINAL", "COLUMNWISE_FROM_ROWWISE_DEQUANTIZED",
     "launch_count", "version", "library",
 ]
@@ -272,3 +272,14 @@ def fp8_quantize_grouped(xs, fmt, scales, qs, stream=None):
     ns = (ctypes.c_int64 * len(xs))(*[t.numel() for t in xs])
     _check(library().fp8_quantize_grouped(len(xs), _ptr_array(xs), ns, _dt(xs[0]), fmt, _p(scales), _ptr_array(qs),
                                           _stream(stream)))
+
+
+def fp8_quantize_current(x, fmt, q_out, margin=0, amax_out=None, scale_out=None, scale_inv_out=None, stream=None):
+    """Current scaling in one call: amax(x), the scale with `margin`, and q_out = codes
+    of x * scale (the cast reduces the amax partials itself; no separate finalize)."""
+    if q_out.dtype != torch.uint8:
+        raise TypeError("q_out must be uint8")
+    if q_out.numel() != x.numel():
+        raise ValueError("q_out must have as many elements as x")
+    _check(library().fp8_quantize_current(_p(x), _dt(x), x.numel(), fmt, margin, _p(q_out), _p(amax_out),
+                                          _p(scale_out), _p(scale_inv_out), _stream(stream)))

@@ -35,6 +35,7 @@ SIGNATURES = {
     "fp8_quantize_mx": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fp8_dequantize_mx": (c_i32, [c_vp, c_vp, c_i32, c_i64, c_i64, c_vp, c_i32, c_vp]),
     "fp8_block128_scales_to_mx": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp]),
+    "fp8_quantize_current": (c_i32, [c_vp, c_i32, c_i64, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fp8_quantize_hybrid": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp]),
     "fp8_quantize_block_cast_transpose": (c_i32, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fp8_amax_grouped": (c_i32, [c_i32, c_vp, c_vp, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),

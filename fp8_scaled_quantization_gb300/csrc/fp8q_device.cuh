@@ -272,6 +272,7 @@ constexpr int kMaxPartials = 8192;
 struct Workspace {
     uint32_t amax[kMaxPartials];
     unsigned long long sat[kMaxPartials];
+    float scratch[4];  // device scalars for calls whose caller passed none
 };
 
 // What a launch that reduced into the workspace leaves to the finalize kernel

@@ -67,6 +67,11 @@ struct FinalizeArgs {
 };
 fp8_status_t launch_finalize(const FinalizeArgs& fa, cudaStream_t st);
 
+// The amax kernel alone: one partial max |x| (fp32 bits) per CTA into
+// ws->amax; *nparts receives their count.  x element-aligned, n >= 0.
+fp8_status_t enqueue_amax_partials(const void* x, fp8_dtype_t dtype, int64_t n, Workspace* ws, cudaStream_t st,
+                                   int* nparts);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_fmt(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
 inline bool valid_dtype(int d) { return d == FP8_DT_BF16 || d == FP8_DT_FP32; }

@@ -5,7 +5,8 @@ stream in ``run()`` and reports the algorithmic bytes one run moves (read
 once + written once, per kernel).  Nothing here computes: every step is a
 call into the CUDA library.
 
-  CurrentScaling     "Megatron FP8" §4/§10: fp8_amax (+ fused scale) -> fp8_quantize
+  CurrentScaling     "Megatron FP8" §4/§10: fp8_quantize_current (amax kernel, then a cast
+                     that derives the scale itself), or fp8_amax (+ scale) -> fp8_quantize
   CurrentCastTranspose  same, with rowwise + columnwise outputs (§6)
   DelayedScaling     §5: per step fp8_quantize (fused amax, saturation count)
                      -> fp8_update_scale_delayed (history ring, window max)
@@ -20,7 +21,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import (AMAX_MAX, E4M3, E5M2, fp8_amax, fp8_dequantize, fp8_quantize, fp8_quantize_block,
-               fp8_quantize_cast_transpose, fp8_quantize_delayed, fp8_update_scale_delayed)
+               fp8_quantize_cast_transpose, fp8_quantize_current, fp8_quantize_delayed, fp8_update_scale_delayed)
 
 
 def _f32(dev, n=1, fill=None):
@@ -53,20 +54,28 @@ def esize(x: torch.Tensor) -> int:
 
 
 class CurrentScaling:
-    """Per-tensor current scaling: amax + scale in one launch, then the cast."""
+    """Per-tensor current scaling: one fp8_quantize_current call (current_call=True),
+    or fp8_amax (amax + scale) followed by fp8_quantize."""
 
-    def __init__(self, x: torch.Tensor, fmt: int = E4M3, margin: int = 0):
-        self.x, self.fmt, self.margin = x, fmt, margin
+    def __init__(self, x: torch.Tensor, fmt: int = E4M3, margin: int = 0, current_call: bool = True):
+        self.x, self.fmt, self.margin, self.current_call = x, fmt, margin, current_call
         dev = x.device
         self.q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
         self.amax, self.scale, self.scale_inv = _f32(dev), _f32(dev), _f32(dev)
 
     def run(self, timer=None):
+        if self.current_call:
+            _t(timer, "quantize_current", lambda: fp8_quantize_current(self.x, self.fmt, self.q, self.margin,
+                                                                       self.amax, self.scale, self.scale_inv))
+            return
         _t(timer, "amax", lambda: fp8_amax(self.x, self.amax, self.fmt, self.margin, self.scale, self.scale_inv))
         _t(timer, "quantize", lambda: fp8_quantize(self.x, self.fmt, self.scale, self.q))
 
     def bytes(self) -> KernelBytes:
         n, b = self.x.numel(), KernelBytes()
+        if self.current_call:  # the amax kernel's read of x and the cast
+            b.add("quantize_current", n * esize(self.x) + n * (esize(self.x) + 1))
+            return b
         b.add("amax", n * esize(self.x))
         b.add("quantize", n * (esize(self.x) + 1))
         return b
@@ -179,8 +188,9 @@ class BlockScaling:
 class GradientQDQ:
     """Per tensor: E5M2 current scaling, then dequantize back to BF16."""
 
-    def __init__(self, xs: list, fmt: int = E5M2, margin: int = 0, keep_outputs: bool = False):
-        self.xs, self.fmt, self.margin = xs, fmt, margin
+    def __init__(self, xs: list, fmt: int = E5M2, margin: int = 0, keep_outputs: bool = False,
+                 current_call: bool = True):
+        self.xs, self.fmt, self.margin, self.current_call = xs, fmt, margin, current_call
         dev = xs[0].device
         n = len(xs) if keep_outputs else 1
         self.q = [torch.empty(xs[0].shape, dtype=torch.uint8, device=dev) for _ in range(n)]
@@ -196,16 +206,23 @@ class GradientQDQ:
     def run_tensor(self, k: int, timer=None):
         x, q, y = self.xs[k], self.q[k % len(self.q)], self.y[k % len(self.y)]
         s, si = self.scale[k:k + 1], self.scale_inv[k:k + 1]
-        _t(timer, "amax", lambda: fp8_amax(x, self.amax[k:k + 1], self.fmt, self.margin, s, si))
-        _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
+        if self.current_call:
+            _t(timer, "quantize_current",
+               lambda: fp8_quantize_current(x, self.fmt, q, self.margin, self.amax[k:k + 1], s, si))
+        else:
+            _t(timer, "amax", lambda: fp8_amax(x, self.amax[k:k + 1], self.fmt, self.margin, s, si))
+            _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
         _t(timer, "dequantize", lambda: fp8_dequantize(q, self.fmt, si, y))
 
     def bytes(self) -> KernelBytes:
         b = KernelBytes()
         for x in self.xs:
             n = x.numel()
-            b.add("amax", n * esize(x))
-            b.add("quantize", n * (esize(x) + 1))
+            if self.current_call:
+                b.add("quantize_current", n * esize(x) + n * (esize(x) + 1))
+            else:
+                b.add("amax", n * esize(x))
+                b.add("quantize", n * (esize(x) + 1))
             b.add("dequantize", n * (1 + 2))
         return b
 

@@ -235,6 +235,25 @@ fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64
                                          void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Current scaling: amax, scale and cast in one call                         */
+/* ------------------------------------------------------------------------ */
+/* "Megatron FP8" §10 (current scaling: the cast's scale comes from the amax
+ * of the tensor being cast) and §4 (amax -> scale with margin -> saturating
+ * cast).  Results are identical to fp8_amax(x, .., scale_out, scale_inv_out)
+ * followed by fp8_quantize(x, .., scale_out, q_out):
+ *   q_out[i] = encode(fl32(x[i] * scale)), scale by the scale rule above.
+ *   amax_out, scale_out, scale_inv_out: device float[1] each, each nullable.
+ * Aligned x and q_out, amax kernel leaving at most 256 partials (about 6M
+ * BF16 elements): two launches, the amax kernel (one partial per CTA) and the
+ * cast, whose CTAs reduce the partials themselves while their own loads of x
+ * are in flight -- no separate finalize.  Larger tensors: the amax kernel,
+ * the one-CTA finalize and the cast (faster there).  Unaligned pointers: the
+ * fp8_amax + fp8_quantize kernels. */
+fp8_status_t fp8_quantize_current(const void* x, fp8_dtype_t dtype, int64_t n, fp8_format_t fmt, int margin,
+                                  uint8_t* q_out, float* amax_out, float* scale_out, float* scale_inv_out,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Hybrid per-direction quantization                                         */
 /* ------------------------------------------------------------------------ */
 /* "[Pytorch][Common] Hybrid quantization #2817": the rowwise and columnwise

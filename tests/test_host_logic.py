@@ -70,6 +70,10 @@ BAD = 0x1000  # never dereferenced: every call below is rejected on the host fir
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 32, 32, BAD, 0, None), 2, "block shape"),
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD, 0, 0, BAD, 7, None), 1, "out_dtype"),
     (lambda L: L.fp8_dequantize(BAD, 0, 4, 4, BAD + 2, 0, 0, BAD, 0, None), 1, "scale_inv not 4-byte"),
+    (lambda L: L.fp8_quantize_current(BAD, 0, -1, 0, 0, BAD, None, None, None, None), 1, "n < 0"),
+    (lambda L: L.fp8_quantize_current(BAD, 0, 10, 0, 200, BAD, None, None, None, None), 1, "margin"),
+    (lambda L: L.fp8_quantize_current(BAD, 0, 10, 4, 0, BAD, None, None, None, None), 1, "unknown format"),
+    (lambda L: L.fp8_quantize_current(None, 0, 10, 0, 0, BAD, None, None, None, None), 1, "is NULL"),
     (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, BAD, BAD, 1, BAD, BAD, 5, None), 1, "columnwise source"),
     (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, BAD, BAD, 3, BAD, BAD, 0, None), 1, "unknown format"),
     (lambda L: L.fp8_quantize_hybrid(BAD, 0, 4, 4, 0, None, BAD, 1, BAD, BAD, 0, None), 1, "scale is NULL"),
@@ -139,7 +143,8 @@ def test_pipeline_byte_accounting_full_size():
     assert b["W5"].total == 32 * 8 * N5
     total = sum(x.total for x in b.values())
     assert 21.0e9 < total < 21.3e9
-    assert sum(x.launches for x in b.values()) == 2 + 2 + (16 + 1) + 2 + 96
+    assert b["W5"].per_kernel["quantize_current"] == (32 * 5 * N5, 32)
+    assert sum(x.launches for x in b.values()) == 1 + 2 + (16 + 1) + 2 + 64  # API calls
 
 
 # ------------------------------------------------------------- multi-rank
@@ -204,3 +209,12 @@ def test_grouped_binding_marshals_and_rejects_host_tensors():
                                                                torch.zeros(32, dtype=torch.uint8)])
     with pytest.raises(ValueError, match="at least len"):
         fq.fp8_amax_grouped(xs, torch.zeros(1))
+
+
+def test_two_call_current_scaling_byte_accounting():
+    from fp8_scaled_quantization_gb300 import pipelines as P
+    x = torch.empty((1024, 1024), dtype=torch.bfloat16, device=torch.device("meta"))
+    b = P.CurrentScaling(x, current_call=False).bytes()
+    assert b.per_kernel == {"amax": (2 * 2 ** 20, 1), "quantize": (3 * 2 ** 20, 1)}
+    g = P.GradientQDQ([x, x], current_call=False).bytes()
+    assert g.per_kernel["amax"] == (2 * 2 * 2 ** 20, 2) and g.per_kernel["dequantize"] == (2 * 3 * 2 ** 20, 2)
