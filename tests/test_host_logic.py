@@ -218,3 +218,17 @@ def test_two_call_current_scaling_byte_accounting():
     assert b.per_kernel == {"amax": (2 * 2 ** 20, 1), "quantize": (3 * 2 ** 20, 1)}
     g = P.GradientQDQ([x, x], current_call=False).bytes()
     assert g.per_kernel["amax"] == (2 * 2 * 2 ** 20, 2) and g.per_kernel["dequantize"] == (2 * 3 * 2 ** 20, 2)
+
+
+def test_input_digests_hash_each_workloads_bytes():
+    import hashlib
+    import bench
+    g = torch.Generator().manual_seed(0)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)  # noqa: E731
+    inp = {"w1": mk(4, 8), "w2": mk(8, 8), "w3": [mk(2, 8), mk(2, 8)], "w4": (mk(4, 4), mk(2, 4)), "w5": [mk(3, 8)]}
+    d = bench.input_digests(inp)
+    h = hashlib.sha256()
+    for t in inp["w3"]:
+        h.update(t.view(torch.int16).numpy().tobytes())
+    assert d["W3"] == h.hexdigest()[:16]
+    assert set(d) == {"W1", "W2", "W3", "W4", "W5"} and len(set(d.values())) == 5
