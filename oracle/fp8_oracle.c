@@ -25,8 +25,8 @@
  *                      scales; "MXFP8 (Blackwell only)": the stored block
  *                      factor of block FP8 is the inverse scale.
  *
- * Readings where the pages are silent or garbled are listed in the design doc of
- * the repository and restated next to the code they govern.
+ * Where the pages are silent or garbled, the reading taken is stated next to
+ * the code it governs.
  *
  * Floating point: every fp32 operation below is a single IEEE-754 binary32
  * operation rounded to nearest-even (compile with -ffp-contract=off, no fast
