@@ -512,7 +512,7 @@ def run_extras_only(args):
     fq.library()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    inp = make_inputs(workload_shapes(1.0), dev, which=("W2", "W4"))
+    inp = make_inputs(workload_shapes(1.0), dev, which=("W1", "W2", "W4"))
     peak, _ = measured_hbm_peak()
     return {"metric": METRIC, "unit": UNIT, "extras": run_extras(inp, peak, reps=max(1, args.steps))}
 

@@ -35,7 +35,10 @@ def mx_input(shape, dtype, seed, dev, specials=True):
     return x.to(dtype).to(dev)
 
 
-SHAPES = [(32, 128), (64, 384), (96, 256), (33, 130), (1, 31), (100, 64), (7, 1000), (256, 4096)]
+# 32-row multiples with 128-column multiples take the 32 x 128-tile kernel,
+# the rest the guarded kernel.
+SHAPES = [(32, 128), (64, 384), (96, 256), (33, 130), (1, 31), (100, 64), (7, 1000), (256, 4096), (128, 128),
+          (384, 256)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -120,3 +123,20 @@ def test_mx_full_size_activation(cuda, oracle):
     del wq
     wqt, wst = oracle.quantize_mx(np.ascontiguousarray(xb.T), E4M3, th)
     assert np.array_equal(s_col.cpu().numpy(), wst) and np.array_equal(q_col.cpu().numpy(), wqt)
+
+
+@pytest.mark.parametrize("which", ["rowwise", "columnwise"])
+def test_mx_single_direction_several_tiles(cuda, oracle, which):
+    x = mx_input((256, 384), torch.bfloat16, 6, cuda)
+    if which == "rowwise":
+        q = torch.empty((256, 384), dtype=torch.uint8, device=cuda)
+        s = torch.empty((256, 12), dtype=torch.uint8, device=cuda)
+        fq.fp8_quantize_mx(x, E5M2, q, s)
+        want = oracle.quantize_mx(host(x), E5M2)
+    else:
+        q = torch.empty((384, 256), dtype=torch.uint8, device=cuda)
+        s = torch.empty((384, 8), dtype=torch.uint8, device=cuda)
+        fq.fp8_quantize_mx(x, E5M2, None, None, q, s)
+        want = oracle.quantize_mx(np.ascontiguousarray(host(x).T), E5M2)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), want[0]) and np.array_equal(s.cpu().numpy(), want[1])
