@@ -1,0 +1,93 @@
+"""Maximum sizes: tensors of more than 2^31 elements, so that every index on
+the device path must be 64-bit.  The oracle (threaded) checks amax, the
+saturation count and every code; the dequantized and transposed outputs are
+checked on samples against the oracle's per-element rule.
+
+About 13 GB of device memory and 9 GB of host memory.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_scaled_quantization_gb300 as fq
+
+from test_gpu_parity import f32_bits, host_bits
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = fq.E4M3, fq.E5M2
+N_BIG = (1 << 31) + 33
+
+
+def big_bf16(shape, seed, dev):
+    """BF16 N(0, 1) * 8 filled in slices (no fp32 copy of the whole tensor)."""
+    x = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    flat = x.view(-1)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    step = 1 << 28
+    for s in range(0, flat.numel(), step):
+        e = min(s + step, flat.numel())
+        flat[s:e] = (torch.randn(e - s, generator=g, device=dev) * 8).to(torch.bfloat16)
+    return x
+
+
+def test_amax_quantize_dequantize_beyond_2_pow_31(cuda, oracle):
+    threads = oracle.default_threads()
+    x = big_bf16((N_BIG,), 71, cuda)
+    x[(1 << 31) + 5] = -300.0   # past the 32-bit index range
+    x[N_BIG - 1] = 1000.0       # the very last element holds the maximum
+    am, s, si = (torch.empty(1, device=cuda) for _ in range(3))
+    fq.fp8_amax(x, am, E4M3, 0, s, si)
+    torch.cuda.synchronize()
+    assert am.item() == 1000.0
+    xb = host_bits(x)
+    ws, wsi = oracle.compute_scale(np.float32(1000.0), E4M3, 0)
+    assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi))
+    # a scale that saturates everything above 100: the count covers the whole range
+    scale = torch.full((1,), 4.48, device=cuda)
+    q = torch.empty(N_BIG, dtype=torch.uint8, device=cuda)
+    am2 = torch.empty(1, device=cuda)
+    sat = torch.empty(1, dtype=torch.int64, device=cuda)
+    fq.fp8_quantize(x, E4M3, scale, q, am2, sat)
+    torch.cuda.synchronize()
+    wq, wsat = oracle.quantize(xb, E4M3, np.float32(4.48), threads)
+    assert sat.item() == wsat and wsat >= 2
+    assert am2.item() == 1000.0
+    assert np.array_equal(q.cpu().numpy(), wq)
+    del wq
+    y = torch.empty(N_BIG, dtype=torch.bfloat16, device=cuda)
+    si2 = torch.full((1,), np.float32(1.0) / np.float32(4.48), device=cuda)
+    fq.fp8_dequantize(q, E4M3, si2, y)
+    torch.cuda.synchronize()
+    idx = torch.cat([torch.randint(0, N_BIG, (1 << 20,), device=cuda),
+                     torch.arange(N_BIG - 4096, N_BIG, device=cuda)])
+    qs = q[idx].cpu().numpy()
+    want = oracle.dequantize(qs, E4M3, si2.cpu().numpy())
+    assert np.array_equal(host_bits(y[idx]), want)
+
+
+def test_cast_transpose_beyond_2_pow_31(cuda, oracle):
+    rows, cols = 16512, 131072  # 2.16e9 elements, 129 x 1024 tiles
+    x = big_bf16((rows, cols), 72, cuda)
+    x[rows - 1, cols - 1] = 512.0
+    scale = torch.full((1,), 0.5, device=cuda)
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((cols, rows), dtype=torch.uint8, device=cuda)
+    am = torch.empty(1, device=cuda)
+    with pytest.raises(fq.Fp8Error) as e:  # the fused amax covers at most 8192 tiles of 128 x 128
+        fq.fp8_quantize_cast_transpose(x, E4M3, scale, q_row, None, am)
+    assert e.value.status == 2
+    fq.fp8_quantize_cast_transpose(x, E4M3, scale, q_row, None)
+    fq.fp8_quantize_cast_transpose(x, E4M3, scale, None, q_col)
+    fq.fp8_amax(x, am)
+    torch.cuda.synchronize()
+    assert am.item() == 512.0
+    g = torch.Generator(device=cuda).manual_seed(3)
+    r = torch.cat([torch.randint(0, rows, (1 << 20,), generator=g, device=cuda),
+                   torch.full((256,), rows - 1, device=cuda)])
+    c = torch.cat([torch.randint(0, cols, (1 << 20,), generator=g, device=cuda),
+                   torch.arange(cols - 256, cols, device=cuda)])
+    wq, _ = oracle.quantize(host_bits(x[r, c]), E4M3, np.float32(0.5))
+    assert np.array_equal(q_row[r, c].cpu().numpy(), wq)
+    assert np.array_equal(q_col[c, r].cpu().numpy(), wq)
