@@ -73,7 +73,7 @@ __device__ __forceinline__ Codes8 col_codes_bf16x8(uint4 v, float scale) {
 }
 
 template <int FMT, bool BF16, bool AMAX, int FMT_COL = FMT, int SRC = kSame>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ scale_ptr,
                       uint8_t* __restrict__ q_row, uint8_t* __restrict__ q_col, int vec_ok,
                       uint32_t* __restrict__ part_amax, const float* __restrict__ scale_col_ptr) {
@@ -83,12 +83,16 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
     const float scale_col = SRC == kSame ? scale : __ldg(scale_col_ptr);
     const float scale_inv_row = SRC == kRowDequant ? __fdiv_rn(1.0f, scale) : 1.0f;
     // Tiles run in reverse order with evict_first loads: after an amax pass over
-    // x (current scaling) the end of x is the part still in L2.
-    const int64_t r0 = (int64_t)(gridDim.y - 1 - blockIdx.y) * kTile, c0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * kTile;
+    // x (current scaling) the end of x is the part still in L2.  One tile per
+    // CTA, except with the fused amax, whose grid is capped at the workspace's
+    // partial slots and walks the tiles with a stride.
     const uint64_t pol = l2_policy_evict_first();
     const int t = threadIdx.x;
     uint32_t am = 0;  // fp32 bits of max |x| seen by this thread
-
+    const int64_t gx = (cols + kTile - 1) / kTile, ntiles = gx * ((rows + kTile - 1) / kTile);
+    for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
+    const int64_t rev = ntiles - 1 - tl;
+    const int64_t r0 = rev / gx * kTile, c0 = rev % gx * kTile;
     const bool full = vec_ok && r0 + kTile <= rows && c0 + kTile <= cols;
     if (full) {
         if constexpr (BF16) {
@@ -113,7 +117,7 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
                     cc8 = col_codes_bf16x8<FMT_COL>(dequant8_bf16<FMT>(c.lo, c.hi, scale_inv_row), scale_col);
                 *reinterpret_cast<uint2*>(&tile[r * 32 + ((cc * 2) ^ (p << 2))]) = make_uint2(cc8.lo, cc8.hi);
             }
-            if constexpr (AMAX) am = fold_u16x2_to_f32bits(m16);
+            if constexpr (AMAX) am = umax(am, fold_u16x2_to_f32bits(m16));
         } else {
             // 32 threads per 512-byte row, 8 rows per pass, 16 passes in two halves.
             const int lane = t & 31, rsub = t >> 5;
@@ -209,11 +213,13 @@ cast_transpose_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols,
             }
         }
     }
+    __syncthreads();  // the shared tile is rewritten by the next tile of this CTA
+    }
 
     if constexpr (AMAX) {
         __shared__ uint32_t red[32];
         const uint32_t bits = block_max_u32(am, red);
-        if (threadIdx.x == 0) part_amax[blockIdx.y * gridDim.x + blockIdx.x] = bits;
+        if (threadIdx.x == 0) part_amax[blockIdx.x] = bits;
     }
 }
 
@@ -246,9 +252,7 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
         return fail(FP8_ERR_INVALID_ARG, "%s: q_row and q_col are both NULL", fn);
     if (n > 0 && x == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: x is NULL", fn);
     if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
-    const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;
-    if (gy > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: rows > %d", fn, 65535 * kTile);
-    if (gx > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "%s: cols too large", fn);
+    const int64_t ntiles = ((cols + kTile - 1) / kTile) * ((rows + kTile - 1) / kTile);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Workspace* ws = nullptr;
@@ -257,13 +261,14 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
         ws = stream_workspace(st, &s);
         if (!ws) return s;
     }
-    dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)(gy > 0 ? gy : 1));
-    if (n == 0) {
-        if (!amax_out) return FP8_OK;
-        grid = dim3(1, 1);  // one guarded CTA with nothing to do but report amax 0
-    }
-    if (amax_out && (int64_t)grid.x * grid.y > kMaxPartials)
-        return fail(FP8_ERR_UNSUPPORTED, "%s: the fused amax supports at most %d tiles of 128 x 128", fn, kMaxPartials);
+    if (n == 0 && !amax_out) return FP8_OK;
+    // One CTA per tile; with the fused amax at most one CTA per partial slot
+    // (n == 0: one CTA with nothing to do but report amax 0).
+    int64_t g = ntiles;
+    if (amax_out && g > kMaxPartials) g = kMaxPartials;
+    if (g > 0x7FFFFFFF) g = 0x7FFFFFFF;
+    if (g < 1) g = 1;
+    const dim3 grid((unsigned)g);
     const int vec_ok = aligned16(x) && (q_row == nullptr || aligned16(q_row)) && (q_col == nullptr || aligned16(q_col)) &&
                        cols % 16 == 0 && rows % 16 == 0;
     const uint8_t* xp = static_cast<const uint8_t*>(x);
@@ -279,7 +284,7 @@ extern "C" fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t d
     if (s != FP8_OK || !am) return s;
     FinalizeArgs fa;
     fa.part_amax = ws->amax;
-    fa.nparts = (int)(grid.x * grid.y);
+    fa.nparts = (int)grid.x;
     fa.amax_out = amax_out;
     fa.fmt = (int)fmt;
     return launch_finalize(fa, st);
@@ -301,12 +306,12 @@ extern "C" fp8_status_t fp8_quantize_hybrid(const void* x, fp8_dtype_t dtype, in
     if (x == nullptr || q_row == nullptr || q_col == nullptr)
         return fail(FP8_ERR_INVALID_ARG, "%s: x / q_row / q_col is NULL", fn);
     if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
-    const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;
-    if (gy > 65535 || gx > 0x7FFFFFFF) return fail(FP8_ERR_UNSUPPORTED, "%s: shape too large", fn);
+    int64_t g = ((cols + kTile - 1) / kTile) * ((rows + kTile - 1) / kTile);
+    if (g > 0x7FFFFFFF) g = 0x7FFFFFFF;
     const int vec_ok = aligned16(x) && aligned16(q_row) && aligned16(q_col) && cols % 16 == 0 && rows % 16 == 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint8_t* xp = static_cast<const uint8_t*>(x);
-    const dim3 grid((unsigned)gx, (unsigned)gy), block(kThreads);
+    const dim3 grid((unsigned)g), block(kThreads);
     uint32_t* none = nullptr;
     const bool deq = source == FP8_COLUMNWISE_FROM_ROWWISE_DEQUANTIZED;
 #define FP8Q_HYB(FR, FC, B)                                                                                           \

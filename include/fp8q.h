@@ -227,8 +227,9 @@ fp8_status_t fp8_quantize_delayed(const void* x, fp8_dtype_t dtype, int64_t n, f
  * Current scaling is fp8_amax(.., scale_out, scale_inv_out) followed by this
  * call.  Interior 128x128 tiles take the vector path when cols % 16 == 0,
  * rows % 16 == 0 and the pointers are 16-byte aligned; edge tiles and other
- * shapes take a guarded element path.  One kernel launch, plus the one-CTA
- * finalize when amax_out is given (then at most 8192 tiles of 128 x 128). */
+ * shapes take a guarded element path.  One kernel launch (one CTA per tile;
+ * with amax_out at most 8192 CTAs, each walking its share of the tiles), plus
+ * the one-CTA finalize when amax_out is given. */
 fp8_status_t fp8_quantize_cast_transpose(const void* x, fp8_dtype_t dtype, int64_t rows,
                                          int64_t cols, fp8_format_t fmt, const float* scale,
                                          uint8_t* q_row, uint8_t* q_col, float* amax_out,

@@ -591,3 +591,23 @@ def test_back_to_back_reductions_do_not_mix(cuda, oracle):
         _, wsat = oracle.quantize(host_bits(small), E4M3, np.float32(1.0))
         assert sat.item() == wsat and f32_bits(am.item()) == f32_bits(oracle.amax(host_bits(small)))
 
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_cast_transpose_fused_amax_walks_tiles(cuda, oracle, dtype):
+    """12416 x 11520 (97 x 90 = 8730 tiles, more than the 8192 partial slots):
+    the fused-amax CTAs each take several tiles."""
+    g = torch.Generator(device="cpu").manual_seed(64)
+    x = (torch.randn((12416, 11520), generator=g) * 3).to(dtype).to(cuda)
+    x[12415, 11519] = -640.0  # exact in BF16 and fp32
+    s = dev_scalar(np.float32(0.5), cuda)
+    q_row = torch.empty((12416, 11520), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((11520, 12416), dtype=torch.uint8, device=cuda)
+    am = torch.empty(1, device=cuda)
+    fq.fp8_quantize_cast_transpose(x, E4M3, s, q_row, q_col, am)
+    torch.cuda.synchronize()
+    assert am.item() == 640.0
+    xb = host_bits(x)
+    wq, _ = oracle.quantize(xb, E4M3, np.float32(0.5), oracle.default_threads())
+    assert np.array_equal(q_row.cpu().numpy(), wq)
+    assert np.array_equal(q_col.cpu().numpy(), np.ascontiguousarray(wq.T))
