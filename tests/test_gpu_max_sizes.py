@@ -88,3 +88,30 @@ def test_cast_transpose_beyond_2_pow_31(cuda, oracle):
     wq, _ = oracle.quantize(host_bits(x[r, c]), E4M3, np.float32(0.5))
     assert np.array_equal(q_row[r, c].cpu().numpy(), wq)
     assert np.array_equal(q_col[c, r].cpu().numpy(), wq)
+
+
+def test_blockwise_beyond_2_pow_31(cuda, oracle):
+    """128 x 128 and 1 x 128 block scaling, and the 1 x 128 blockwise dequantize,
+    on 16512 x 131072 BF16; the last 256 rows (offsets past 2^31) are checked
+    code by code and scale by scale against the oracle."""
+    rows, cols = 16512, 131072
+    x = big_bf16((rows, cols), 73, cuda)
+    tail = slice(rows - 256, rows)
+    xt = host_bits(x[tail])
+    for br in (128, 1):
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+        si = torch.empty((-(-rows // br), cols // 128), dtype=torch.float32, device=cuda)
+        fq.fp8_quantize_block(x, br, 128, E4M3, q, si)
+        torch.cuda.synchronize()
+        wq, wsi = oracle.quantize_block(xt, br, 128, E4M3, oracle.default_threads())
+        assert np.array_equal(q[tail].cpu().numpy(), wq), br
+        sit = si[(rows - 256) // br:] if br == 128 else si[tail]
+        assert np.array_equal(sit.cpu().numpy().view(np.uint32), wsi.view(np.uint32)), br
+        if br == 1:
+            y = torch.empty((rows, cols), dtype=torch.bfloat16, device=cuda)
+            fq.fp8_dequantize(q, E4M3, si, y, 1, 128)
+            torch.cuda.synchronize()
+            wy = oracle.dequantize(wq, E4M3, wsi, 1, 128, threads=oracle.default_threads())
+            assert np.array_equal(host_bits(y[tail]), wy)
+            del y
+        del q, si
