@@ -165,7 +165,8 @@ def fp8_quantize(x, fmt, scale, q_out, amax_out=None, sat_count_out=None, stream
 
 def fp8_quantize_delayed(x, fmt, scale, scale_inv, q_out, amax_history, step, algo=AMAX_MAX, margin=0,
                          amax_out=None, sat_count_out=None, stream=None):
-    """One delayed-scaling step in one launch: q_out = codes of x * scale, then
+    """One delayed-scaling step in one call (the cast, then a one-CTA finalize):
+    q_out = codes of x * scale, then
     amax(x) goes into amax_history[step % len] and scale / scale_inv are
     overwritten with the scale of the next step."""
     if q_out.dtype != torch.uint8 or q_out.numel() != x.numel():
@@ -261,7 +262,7 @@ def fp8_amax_grouped(xs, amax_out=None, fmt=E4M3, margin=0, scale_out=None, scal
 
 
 def fp8_quantize_grouped(xs, fmt, scales, qs, stream=None):
-    """qs[i] = codes of xs[i] * scales[i] for up to 128 tensors in one launch."""
+    """qs[i] = codes of xs[i] * scales[i] for up to 128 tensors in one kernel launch."""
     if not xs or len(xs) != len(qs) or len({t.dtype for t in xs}) != 1:
         raise ValueError("xs and qs must be equally long lists; xs of one dtype")
     for x, q in zip(xs, qs):

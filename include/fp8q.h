@@ -186,8 +186,9 @@ fp8_status_t fp8_quantize(const void* x, fp8_dtype_t dtype, int64_t n, fp8_forma
 /* ------------------------------------------------------------------------ */
 /* "Megatron FP8" §5: per step, cast with the scale derived from the amax
  * history, record this step's amax into slot step % history_len, and derive
- * the scale of the next step -- here in one launch: the last CTA of the cast
- * performs the update of fp8_update_scale_delayed.
+ * the scale of the next step -- here in one call: the cast (with fused amax
+ * and saturation count) and a one-CTA finalize that performs the update of
+ * fp8_update_scale_delayed.
  *
  * Equivalent, bit for bit, to
  *   fp8_quantize(x, .., scale, q_out, tmp_amax, sat_count_out)

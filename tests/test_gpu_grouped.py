@@ -3,7 +3,7 @@ oracle and against the per-tensor entry points.
 
 "Megatron FP8" §21: each expert of an MoE layer keeps its own per-tensor
 scaling state; the grouped calls compute every tensor's amax, current scale
-and codes in one launch each.
+and codes in one kernel launch each (plus one finalize for the amax).
 """
 from __future__ import annotations
 
