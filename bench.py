@@ -455,6 +455,18 @@ def run_extras(inp, peak, reps=10):
     out["block_cast_transpose"] = row(us, na * 2 + 2 * (na + 4 * na // 128),
                                       "E4M3 1x128 rowwise + 128x1 columnwise (transposed), 16384x7168 BF16")
     del qr, sr, qc, sc
+    # FP32 inputs (master weights): the cast and current scaling of 8192 x 4096 fp32
+    xf = inp["w2"][:, :4096].float().contiguous()
+    nf = xf.numel()
+    qf = torch.empty(xf.shape, dtype=torch.uint8, device=dev)
+    sf = torch.full((1,), 0.25, device=dev)
+    af, sif = torch.empty(1, device=dev), torch.empty(1, device=dev)
+    out["fp32_quantize"] = row(timed(lambda: fq.fp8_quantize(xf, fq.E4M3, sf, qf)), nf * 5,
+                               "FP32 8192x4096 -> E4M3 codes, given scale")
+    out["fp32_current_scaling"] = row(timed(lambda: fq.fp8_quantize_current(xf, fq.E4M3, qf, 0, af, sf, sif)),
+                                      nf * 5, "FP32 8192x4096 current scaling (amax + finalize + cast); "
+                                      "compulsory 5 B/element")
+    del xf, qf
     # W1 (1024 x 1024, 2 MB) is launch- and L2-bound: 20 current-scaling calls
     # captured in one CUDA graph, replayed with a warm L2
     x1 = inp["w1"]
@@ -503,6 +515,19 @@ def run_extras(inp, peak, reps=10):
                                          "64 BF16 tensors [128..2047, 7168]: amax+scale+cast, grouped (3 launches)")
     out["per_tensor_current_scaling"] = row(timed(per_tensor), nbytes,
                                             "the same 64 tensors, per-tensor calls (192 launches)")
+    del xs, qs
+    # FP32 master-weight shards: 32 tensors [512..1535, 4096] fp32, grouped
+    rows32 = torch.randint(512, 1536, (32,), generator=g, device=dev).tolist()
+    ws32 = [torch.randn((int(rr), 4096), generator=g, device=dev) for rr in rows32]
+    qs32 = [torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in ws32]
+    a32, s32, si32 = (torch.empty(32, device=dev) for _ in range(3))
+
+    def grouped32():
+        fq.fp8_amax_grouped(ws32, a32, fq.E4M3, 0, s32, si32)
+        fq.fp8_quantize_grouped(ws32, fq.E4M3, s32, qs32)
+
+    out["grouped_fp32_master_weights"] = row(timed(grouped32), sum(t.numel() * 5 for t in ws32),
+                                             "32 FP32 tensors [512..1535, 4096]: amax+scale+cast, grouped")
     return out
 
 
