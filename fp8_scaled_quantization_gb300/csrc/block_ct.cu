@@ -48,9 +48,9 @@ block_ct_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
     __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];  // columnwise codes, swizzled
     __shared__ uint32_t colmax[16][kTile];                       // per row-group partial column amax (f32 bits)
     __shared__ float colscale[kTile];
-    const int64_t r0 = (int64_t)blockIdx.y * kTile, c0 = (int64_t)blockIdx.x * kTile;
-    const int t = threadIdx.x, lane = t & 31, cc = t & 15, rsub = t >> 4;
     const int64_t nbr_row = cols / 128, nbr_col = rows / 128;
+    const int64_t r0 = (int64_t)blockIdx.x / nbr_row * kTile, c0 = (int64_t)blockIdx.x % nbr_row * kTile;
+    const int t = threadIdx.x, lane = t & 31, cc = t & 15, rsub = t >> 4;
 
     uint4 v[8];  // v[p]: row p * 16 + rsub, columns cc * 8 .. cc * 8 + 7
 #pragma unroll
@@ -223,10 +223,10 @@ fp8_status_t launch_bct(const uint8_t* x, bool bf16, int64_t rows, int64_t cols,
                         uint8_t* q_col, float* si_col, cudaStream_t st) {
     const char* w = "fp8_quantize_block_cast_transpose";
     const bool fast = bf16 && rows % kTile == 0 && cols % kTile == 0 && aligned16(x) && (!q_row || aligned16(q_row)) &&
-                      (!q_col || aligned16(q_col)) && rows / kTile <= 65535;
+                      (!q_col || aligned16(q_col)) && (rows / kTile) * (cols / kTile) <= 0x7FFFFFFF;
     if (fast)
-        return launch(w, block_ct_kernel<FMT>, dim3((unsigned)(cols / kTile), (unsigned)(rows / kTile)), dim3(kThreads), st,
-                      x, rows, cols, q_row, si_row, q_col, si_col);
+        return launch(w, block_ct_kernel<FMT>, dim3((unsigned)((rows / kTile) * (cols / kTile))), dim3(kThreads), st, x,
+                      rows, cols, q_row, si_row, q_col, si_col);
     const int64_t cap = (int64_t)sm_count() * 8;
     const int64_t one = 1;
     if (q_row) {

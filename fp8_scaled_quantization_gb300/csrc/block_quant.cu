@@ -31,7 +31,8 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
     pdl_begin();
     __shared__ uint32_t red[32];
     __shared__ float s_scale;
-    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int64_t bid = blockIdx.x;  // block (bid / nbc, bid % nbc) of the row-major block grid
+    const int64_t r0 = bid / nbc * 128, c0 = bid % nbc * 128;
     const int t = threadIdx.x;
     const bool full = vec_ok && r0 + 128 <= rows && c0 + 128 <= cols;
 
@@ -51,7 +52,7 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
             float sc, si;  // a NaN amax (bits above Inf) gets scale 1 from the scale rule
             scale_from_amax<FMT>(__uint_as_float(bits), 0, &sc, &si);
             s_scale = sc;
-            scale_inv[blockIdx.y * nbc + blockIdx.x] = si;
+            scale_inv[bid] = si;
         }
         __syncthreads();
         const float scale = s_scale;
@@ -84,7 +85,7 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
         float sc, si;
         scale_from_amax<FMT>(__uint_as_float(bits), 0, &sc, &si);
         s_scale = sc;
-        scale_inv[blockIdx.y * nbc + blockIdx.x] = si;
+        scale_inv[bid] = si;
     }
     __syncthreads();
     const float scale = s_scale;
@@ -201,7 +202,7 @@ fp8_status_t launch_block(const uint8_t* x, bool bf16, int64_t rows, int64_t col
     if (br == 128) {
         const int64_t nbr = (rows + 127) / 128;
         const int vec_ok = aligned16(x) && aligned16(q) && cols % 16 == 0;
-        const dim3 grid((unsigned)nbc, (unsigned)nbr);
+        const dim3 grid((unsigned)(nbc * nbr));
         if (bf16) return launch(w, block128_kernel<FMT, true>, grid, dim3(kThreads), st, x, rows, cols, q, si, nbc, vec_ok);
         return launch(w, block128_kernel<FMT, false>, grid, dim3(kThreads), st, x, rows, cols, q, si, nbc, vec_ok);
     }
@@ -238,7 +239,8 @@ extern "C" fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int
         return fail(FP8_ERR_INVALID_ARG, "%s: x / q_out / scale_inv_out is NULL", fn);
     if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
     if (reinterpret_cast<uintptr_t>(scale_inv_out) % 4) return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv_out not 4-byte aligned", fn);
-    if (block_rows == 128 && (rows + 127) / 128 > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: rows too large", fn);
+    if (block_rows == 128 && ((rows + 127) / 128) * ((cols + 127) / 128) > 0x7FFFFFFFLL)
+        return fail(FP8_ERR_UNSUPPORTED, "%s: too many blocks", fn);
     if (rows * ((cols + 127) / 128) / 16 > 0x7FFFFFFFLL) return fail(FP8_ERR_UNSUPPORTED, "%s: too many tiles", fn);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

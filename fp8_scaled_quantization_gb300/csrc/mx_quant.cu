@@ -60,7 +60,8 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
     pdl_begin();
     constexpr int kPad = kTileC + 2;  // row stride in BF16 elements (65 words: conflict-free column reads)
     __shared__ __align__(16) uint16_t tile[kTileR * kPad];
-    const int64_t r0 = (int64_t)blockIdx.y * kTileR, c0 = (int64_t)blockIdx.x * kTileC;
+    const int64_t gx = cols / kTileC;  // tile (blockIdx.x / gx, blockIdx.x % gx)
+    const int64_t r0 = (int64_t)blockIdx.x / gx * kTileR, c0 = (int64_t)blockIdx.x % gx * kTileC;
     const int t = threadIdx.x, lane = t & 31;
     const int cc = t & 15, rsub = t >> 4;  // 16 threads per 256-byte row
     uint4 v[2];
@@ -266,9 +267,10 @@ fp8_status_t launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, 
                        uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
     const char* w = "fp8_quantize_mx";
     const bool fast = bf16 && rows % kTileR == 0 && cols % kTileC == 0 && aligned16(x) &&
-                      (!q_row || aligned16(q_row)) && (!q_col || aligned16(q_col)) && rows / kTileR <= 65535;
+                      (!q_row || aligned16(q_row)) && (!q_col || aligned16(q_col)) &&
+                      (rows / kTileR) * (cols / kTileC) <= 0x7FFFFFFF;
     if (fast) {
-        const dim3 grid((unsigned)(cols / kTileC), (unsigned)(rows / kTileR));
+        const dim3 grid((unsigned)((rows / kTileR) * (cols / kTileC)));
         return launch(w, mx_tile_kernel<FMT>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col, s_col);
     }
     const int64_t cap = (int64_t)sm_count() * 8;

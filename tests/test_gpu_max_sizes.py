@@ -115,3 +115,38 @@ def test_blockwise_beyond_2_pow_31(cuda, oracle):
             assert np.array_equal(host_bits(y[tail]), wy)
             del y
         del q, si
+
+
+def test_tall_tensors_past_65535_row_tiles(cuda, oracle):
+    """Shapes with more than 65535 rows of tiles (the kernels index tiles
+    linearly): MXFP8 (32-row tiles), 128 x 128 blocks and the blockwise
+    cast-transpose (128-row tiles); the last rows against the oracle."""
+    rows = 65536 * 32 + 128  # 2,097,280 rows of MX tiles
+    x = big_bf16((rows, 128), 74, cuda)
+    q = torch.empty((rows, 128), dtype=torch.uint8, device=cuda)
+    s = torch.empty((rows, 4), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_mx(x, E4M3, q, s)
+    torch.cuda.synchronize()
+    wq, ws = oracle.quantize_mx(host_bits(x[-256:]), E4M3)
+    assert np.array_equal(q[-256:].cpu().numpy(), wq) and np.array_equal(s[-256:].cpu().numpy(), ws)
+    del x, q, s
+    rows = 65536 * 128 + 256  # 8,388,864 rows: 65538 row blocks of 128
+    x = big_bf16((rows, 128), 75, cuda)
+    tail = host_bits(x[-256:])
+    q = torch.empty((rows, 128), dtype=torch.uint8, device=cuda)
+    si = torch.empty((rows // 128, 1), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block(x, 128, 128, E4M3, q, si)
+    torch.cuda.synchronize()
+    wq, wsi = oracle.quantize_block(tail, 128, 128, E4M3)
+    assert np.array_equal(q[-256:].cpu().numpy(), wq) and np.array_equal(si[-2:].cpu().numpy(), wsi)
+    q_row = torch.empty((rows, 128), dtype=torch.uint8, device=cuda)
+    s_row = torch.empty((rows, 1), dtype=torch.float32, device=cuda)
+    q_col = torch.empty((128, rows), dtype=torch.uint8, device=cuda)
+    s_col = torch.empty((128, rows // 128), dtype=torch.float32, device=cuda)
+    fq.fp8_quantize_block_cast_transpose(x, E4M3, q_row, s_row, q_col, s_col)
+    torch.cuda.synchronize()
+    wq, wsi = oracle.quantize_block(tail, 1, 128, E4M3)
+    assert np.array_equal(q_row[-256:].cpu().numpy(), wq) and np.array_equal(s_row[-256:].cpu().numpy(), wsi)
+    wqt, wst = oracle.quantize_block(np.ascontiguousarray(tail.T), 1, 128, E4M3)
+    assert np.array_equal(q_col[:, -256:].cpu().numpy(), wqt)
+    assert np.array_equal(s_col[:, -2:].cpu().numpy(), wst)
