@@ -7,9 +7,10 @@
 //
 // Decoding is exact: E4M3 pairs go through cvt.rn.f16x2.e4m3x2 (every E4M3FN
 // value is a binary16 value); an E5M2 code is the upper byte of a binary16.
-// Per-tensor: flat grid-stride, 16 codes in / 32 (BF16) or 64 (fp32) bytes
-// out per thread and unit.  Block-scaled: one CTA row per tensor row, the
-// scale of each 16-code chunk read from the block grid.
+// Both paths work in items of one 16-byte output piece per thread (8 codes
+// for BF16, 4 for fp32), so every warp store covers 512 contiguous bytes.
+// Per-tensor: one chunk of 256 x 16 items per CTA.  Block-scaled: grid.y walks
+// rows, the scale of each item read from the block grid.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -17,7 +18,6 @@ namespace fp8q {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnits = 8;  // 16-code units per thread in the per-tensor kernel
 
 // 4 codes (one word) -> 4 products in fp32.
 template <int FMT>
@@ -30,32 +30,6 @@ __device__ __forceinline__ void decode4(uint32_t w, float si, float* o) {
     o[3] = __fmul_rn(f16_hi_to_f32(h23), si);
 }
 
-// 16 codes -> stores at y (element offset `e` of the output).
-template <int FMT, bool OUT_BF16>
-__device__ __forceinline__ void dequant16(uint4 c, float si, uint8_t* y, int64_t e) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    if constexpr (OUT_BF16) {
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float f[4];
-            decode4<FMT>(w[i], si, f);
-            o[2 * i] = f32x2_to_bf16x2(f[0], f[1]);
-            o[2 * i + 1] = f32x2_to_bf16x2(f[2], f[3]);
-        }
-        stg_stream(y + e * 2, make_uint4(o[0], o[1], o[2], o[3]));
-        stg_stream(y + e * 2 + 16, make_uint4(o[4], o[5], o[6], o[7]));
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float f[4];
-            decode4<FMT>(w[i], si, f);
-            stg_stream(y + (e + 4 * i) * 4, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                                                       __float_as_uint(f[2]), __float_as_uint(f[3])));
-        }
-    }
-}
-
 template <int FMT, bool OUT_BF16>
 __device__ __forceinline__ void dequant_one(uint8_t code, float si, uint8_t* y, int64_t e) {
     float f[4];
@@ -64,29 +38,55 @@ __device__ __forceinline__ void dequant_one(uint8_t code, float si, uint8_t* y, 
     else reinterpret_cast<float*>(y)[e] = f[0];
 }
 
-// Per-tensor scale, q and y 16-byte aligned (any n).  Each CTA owns one chunk
-// of 256 * kUnits 16-code units and issues all its loads first.
+// Per-tensor path: each item is the codes of one 16-byte output piece (8 codes
+// for BF16, 4 for fp32), so a warp's store covers 512 contiguous bytes and its
+// load 256 / 128 contiguous bytes; 16 items in flight per thread, one chunk of
+// 256 * 16 items per CTA.  (Two 16-byte stores per thread at a 32-byte stride,
+// each filling half of every sector it touches, measured 26% slower.)
+constexpr int kItems = 16;
+
 template <int FMT, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads)
 dequant_tensor_kernel(const uint8_t* __restrict__ q, int64_t n, const float* __restrict__ scale_inv,
                       uint8_t* __restrict__ y) {
     pdl_begin();
-    const int64_t nunits = n / 16;
-    const int64_t ubase = (int64_t)blockIdx.x * kThreads * kUnits + threadIdx.x;
-    uint4 c[kUnits];
+    constexpr int kCodes = OUT_BF16 ? 8 : 4;
+    const int64_t nitems = n / kCodes;
+    const int64_t ibase = (int64_t)blockIdx.x * kThreads * kItems + threadIdx.x;
+    uint32_t c[kItems][kCodes / 4];
 #pragma unroll
-    for (int k = 0; k < kUnits; ++k) {
-        const int64_t u = ubase + (int64_t)k * kThreads;
-        if (u < nunits) c[k] = ldg_stream(q + u * 16);
+    for (int k = 0; k < kItems; ++k) {
+        const int64_t i = ibase + (int64_t)k * kThreads;
+        if (i < nitems) {
+            if constexpr (OUT_BF16) {
+                const uint2 v = __ldcs(reinterpret_cast<const uint2*>(q) + i);
+                c[k][0] = v.x;
+                c[k][kCodes / 4 - 1] = v.y;
+            } else {
+                c[k][0] = __ldcs(reinterpret_cast<const unsigned int*>(q) + i);
+            }
+        }
     }
     const float si = __ldg(scale_inv);
 #pragma unroll
-    for (int k = 0; k < kUnits; ++k) {
-        const int64_t u = ubase + (int64_t)k * kThreads;
-        if (u < nunits) dequant16<FMT, OUT_BF16>(c[k], si, y, u * 16);
+    for (int k = 0; k < kItems; ++k) {
+        const int64_t i = ibase + (int64_t)k * kThreads;
+        if (i >= nitems) continue;
+        if constexpr (OUT_BF16) {
+            float a[4], b[4];
+            decode4<FMT>(c[k][0], si, a);
+            decode4<FMT>(c[k][kCodes / 4 - 1], si, b);
+            stg_stream(y + i * 16, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
+                                              f32x2_to_bf16x2(b[0], b[1]), f32x2_to_bf16x2(b[2], b[3])));
+        } else {
+            float a[4];
+            decode4<FMT>(c[k][0], si, a);
+            stg_stream(y + i * 16, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                              __float_as_uint(a[3])));
+        }
     }
     if (blockIdx.x == gridDim.x - 1)
-        for (int64_t e = nunits * 16 + threadIdx.x; e < n; e += kThreads) dequant_one<FMT, OUT_BF16>(q[e], si, y, e);
+        for (int64_t e = nitems * kCodes + threadIdx.x; e < n; e += kThreads) dequant_one<FMT, OUT_BF16>(q[e], si, y, e);
 }
 
 // Any layout: grid.y walks rows, threads walk columns.  `vec` selects 16-code
@@ -99,13 +99,26 @@ dequant_rows_kernel(const uint8_t* __restrict__ q, int64_t rows, int64_t cols, c
     pdl_begin();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
         const float* srow = br > 0 ? scale_inv + (br == 1 ? r : (r >> 7)) * nbc : scale_inv;
-        if (vec) {
-            const int64_t nch = cols / 16;
-            for (int64_t ch = (int64_t)blockIdx.x * kThreads + threadIdx.x; ch < nch; ch += (int64_t)gridDim.x * kThreads) {
-                const int64_t c = ch * 16;
+        if (vec) {  // items of one 16-byte output piece, as in dequant_tensor_kernel
+            constexpr int kCodes = OUT_BF16 ? 8 : 4;
+            const int64_t nit = cols / kCodes;
+            for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < nit; it += (int64_t)gridDim.x * kThreads) {
+                const int64_t c = it * kCodes;
                 const float si = __ldg(br > 0 ? srow + (c >> 7) : srow);
                 const int64_t e = r * cols + c;
-                dequant16<FMT, OUT_BF16>(ldg_stream(q + e), si, y, e);
+                float a[4];
+                if constexpr (OUT_BF16) {
+                    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(q + e));
+                    float b[4];
+                    decode4<FMT>(v.x, si, a);
+                    decode4<FMT>(v.y, si, b);
+                    stg_stream(y + e * 2, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
+                                                     f32x2_to_bf16x2(b[0], b[1]), f32x2_to_bf16x2(b[2], b[3])));
+                } else {
+                    decode4<FMT>(__ldcs(reinterpret_cast<const unsigned int*>(q + e)), si, a);
+                    stg_stream(y + e * 4, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                                     __float_as_uint(a[3])));
+                }
             }
         } else {
             for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < cols; c += (int64_t)gridDim.x * kThreads) {
@@ -124,12 +137,13 @@ fp8_status_t launch_deq(const uint8_t* q, int64_t rows, int64_t cols, const floa
     const int64_t n = rows * cols;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (br == 0 && aligned16(q) && aligned16(y)) {
-        int64_t grid = (n / 16 + (int64_t)kThreads * kUnits - 1) / ((int64_t)kThreads * kUnits);
+        const int64_t nitems = n / (OUT_BF16 ? 8 : 4);
+        int64_t grid = (nitems + (int64_t)kThreads * kItems - 1) / ((int64_t)kThreads * kItems);
         if (grid < 1) grid = 1;
         return launch(w, dequant_tensor_kernel<FMT, OUT_BF16>, dim3((unsigned)grid), dim3(kThreads), st, q, n, si, y);
     }
     const int vec = aligned16(q) && aligned16(y) && cols % 16 == 0;
-    const int64_t per_row = vec ? cols / 16 : cols;
+    const int64_t per_row = vec ? cols / (OUT_BF16 ? 8 : 4) : cols;
     int64_t gx = (per_row + kThreads - 1) / kThreads;
     if (gx < 1) gx = 1;
     if (gx > cap) gx = cap;

@@ -111,58 +111,48 @@ grouped_finalize_kernel(const __grid_constant__ GroupTable t, const uint32_t* __
     }
 }
 
-// Cast: one chunk of 4 (BF16) / 2 (fp32) 16-element units per thread per CTA,
-// tensor i scaled by scale[i]; x and q pointers 16-byte aligned.
+// Cast: one chunk of 8 items of one 16-byte load (8 BF16 / 4 fp32 elements)
+// per thread per CTA -- a warp loads 512 contiguous bytes -- tensor i scaled by
+// scale[i]; x and q pointers 16-byte aligned.
 template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 5)
 grouped_quantize_kernel(const __grid_constant__ GroupTable t, const float* __restrict__ scales) {
     pdl_begin();
-    constexpr int kUnits = BF16 ? 4 : 2, kLoads = BF16 ? 2 : 4;
+    constexpr int kItems = 8, kPer = BF16 ? 8 : 4;
     const int64_t chunk = blockIdx.x;
     const int i = find_tensor(t, chunk);
     const int64_t local = chunk - t.chunk_begin[i];
     const uint8_t* x = t.x[i];
     uint8_t* q = t.q[i];
-    const int64_t n = t.n[i], nunits = n / 16;
+    const int64_t n = t.n[i], nitems = n / kPer;
     const float scale = scales[i];
-    const int64_t ub = local * kThreads * kUnits + threadIdx.x;
-    uint4 v[kUnits][kLoads];
+    const int64_t ib = local * kThreads * kItems + threadIdx.x;
+    uint4 v[kItems];
 #pragma unroll
-    for (int k = 0; k < kUnits; ++k) {
-        const int64_t u = ub + (int64_t)k * kThreads;
-        if (u < nunits) {
-#pragma unroll
-            for (int h = 0; h < kLoads; ++h) v[k][h] = ldg_stream(x + u * (BF16 ? 32 : 64) + h * 16);
-        }
+    for (int k = 0; k < kItems; ++k) {
+        const int64_t it = ib + (int64_t)k * kThreads;
+        if (it < nitems) v[k] = ldg_stream(x + it * 16);
     }
 #pragma unroll
-    for (int k = 0; k < kUnits; ++k) {
-        const int64_t u = ub + (int64_t)k * kThreads;
-        if (u >= nunits) break;
+    for (int k = 0; k < kItems; ++k) {
+        const int64_t it = ib + (int64_t)k * kThreads;
+        if (it >= nitems) break;
         if constexpr (BF16) {
-            Codes8 cd[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t m;
-                cd[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
-                if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[k][h], scale, &cd[h]);
-            }
-            stg_stream(q + u * 16, make_uint4(cd[0].lo, cd[0].hi, cd[1].lo, cd[1].hi));
+            uint32_t m;
+            Codes8 cd = cvt_bf16x8<FMT>(v[k], scale, &m);
+            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[k], scale, &cd);
+            stg_stream(q + it * 8, make_uint2(cd.lo, cd.hi));
         } else {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
-                                       __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
-                uint32_t m;
-                w[h] = cvt_f32x4<FMT>(f, scale, &m);
-                if (chunk_needs_fixup<FMT, false>(m, scale)) fixup_f32x4<FMT>(f, scale, &w[h]);
-            }
-            stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
+            const float4 f = make_float4(__uint_as_float(v[k].x), __uint_as_float(v[k].y), __uint_as_float(v[k].z),
+                                         __uint_as_float(v[k].w));
+            uint32_t m;
+            uint32_t w = cvt_f32x4<FMT>(f, scale, &m);
+            if (chunk_needs_fixup<FMT, false>(m, scale)) fixup_f32x4<FMT>(f, scale, &w);
+            __stcs(reinterpret_cast<unsigned int*>(q + it * 4), w);
         }
     }
-    if (local == 0) {  // elements after the last full unit of tensor i
-        for (int64_t e = nunits * 16 + threadIdx.x; e < n; e += kThreads) {
+    if (local == 0) {  // elements after the last full item of tensor i
+        for (int64_t e = nitems * kPer + threadIdx.x; e < n; e += kThreads) {
             const float xv = BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16)
                                   : reinterpret_cast<const float*>(x)[e];
             uint32_t s;
@@ -255,7 +245,7 @@ extern "C" fp8_status_t fp8_quantize_grouped(int count, const void* const* xs, c
     const bool bf16 = dtype == FP8_DT_BF16;
     GroupTable t;
     fp8_status_t s = FP8_OK;
-    if (!fill_table(&t, count, xs, qs, ns, (int64_t)kThreads * (bf16 ? 4 : 2) * 16, fn, &s)) return s;
+    if (!fill_table(&t, count, xs, qs, ns, (int64_t)kThreads * 8 * (bf16 ? 8 : 4), fn, &s)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid((unsigned)t.chunk_begin[count]), block(kThreads);
     if (fmt == FP8_E4M3)

@@ -186,57 +186,57 @@ mx_dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, 
 }
 
 // Fast MX dequantize: cols % 32 == 0 and 16-byte aligned q / y, so the block of
-// flat element e is e / 32; each thread converts 16-code units, 8 in flight,
-// loading each unit's scale byte together with its codes.
+// flat element e is e / 32.  Each item is the codes of one 16-byte output
+// piece (8 codes for BF16, 4 for fp32; always inside one 32-element block), so
+// every warp store covers 512 contiguous bytes; 16 items in flight per thread,
+// each item's E8M0 byte loaded together with its codes.
 template <int FMT, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 mx_dequant_vec_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int64_t n,
                       uint8_t* __restrict__ y) {
     pdl_begin();
-    constexpr int kU = 8;
-    const int64_t nunits = n / 16;
-    const int64_t ub = (int64_t)blockIdx.x * kThreads * kU + threadIdx.x;
-    uint4 c[kU];
-    uint32_t code[kU];
+    constexpr int kI = 16, kCodes = OUT_BF16 ? 8 : 4, kPerBlock = 32 / kCodes;
+    const int64_t nitems = n / kCodes;
+    const int64_t ib = (int64_t)blockIdx.x * kThreads * kI + threadIdx.x;
+    uint32_t c[kI][kCodes / 4];
+    uint32_t code[kI];
 #pragma unroll
-    for (int k = 0; k < kU; ++k) {
-        const int64_t u = ub + (int64_t)k * kThreads;
-        if (u < nunits) {
-            c[k] = ldg_stream(q + u * 16);
-            code[k] = s[u >> 1];  // 16-code unit u lies in 32-element block u / 2
+    for (int k = 0; k < kI; ++k) {
+        const int64_t i = ib + (int64_t)k * kThreads;
+        if (i < nitems) {
+            if constexpr (OUT_BF16) {
+                const uint2 v = __ldcs(reinterpret_cast<const uint2*>(q) + i);
+                c[k][0] = v.x;
+                c[k][kCodes / 4 - 1] = v.y;
+            } else {
+                c[k][0] = __ldcs(reinterpret_cast<const unsigned int*>(q) + i);
+            }
+            code[k] = s[i / kPerBlock];
         }
     }
 #pragma unroll
-    for (int k = 0; k < kU; ++k) {
-        const int64_t u = ub + (int64_t)k * kThreads;
-        if (u >= nunits) continue;
+    for (int k = 0; k < kI; ++k) {
+        const int64_t i = ib + (int64_t)k * kThreads;
+        if (i >= nitems) continue;
         const float m = code[k] == 0xFFu ? __uint_as_float(0x7FFFFFFFu)
                                          : (code[k] == 0u ? __uint_as_float(0x00400000u) : exp2i((int)code[k] - 127));
-        const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
-        float f[16];
+        float f[kCodes];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t h01 = fp8x2_to_f16x2<FMT>(w[i] & 0xFFFFu), h23 = fp8x2_to_f16x2<FMT>(w[i] >> 16);
-            f[4 * i + 0] = __fmul_rn(f16_lo_to_f32(h01), m);
-            f[4 * i + 1] = __fmul_rn(f16_hi_to_f32(h01), m);
-            f[4 * i + 2] = __fmul_rn(f16_lo_to_f32(h23), m);
-            f[4 * i + 3] = __fmul_rn(f16_hi_to_f32(h23), m);
+        for (int w = 0; w < kCodes / 4; ++w) {
+            const uint32_t h01 = fp8x2_to_f16x2<FMT>(c[k][w] & 0xFFFFu), h23 = fp8x2_to_f16x2<FMT>(c[k][w] >> 16);
+            f[4 * w + 0] = __fmul_rn(f16_lo_to_f32(h01), m);
+            f[4 * w + 1] = __fmul_rn(f16_hi_to_f32(h01), m);
+            f[4 * w + 2] = __fmul_rn(f16_lo_to_f32(h23), m);
+            f[4 * w + 3] = __fmul_rn(f16_hi_to_f32(h23), m);
         }
         if constexpr (OUT_BF16) {
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = f32x2_to_bf16x2(f[2 * i], f[2 * i + 1]);
-            stg_stream(y + u * 32, make_uint4(o[0], o[1], o[2], o[3]));
-            stg_stream(y + u * 32 + 16, make_uint4(o[4], o[5], o[6], o[7]));
+            stg_stream(y + i * 16, make_uint4(f32x2_to_bf16x2(f[0], f[1]), f32x2_to_bf16x2(f[2], f[3]),
+                                              f32x2_to_bf16x2(f[4], f[5]), f32x2_to_bf16x2(f[6], f[7])));
         } else {
+            uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    o[j] = isnan(f[4 * i + j]) ? 0x7FFFFFFFu : __float_as_uint(f[4 * i + j]);
-                stg_stream(y + (u * 16 + 4 * i) * 4, make_uint4(o[0], o[1], o[2], o[3]));
-            }
+            for (int j = 0; j < 4; ++j) o[j] = isnan(f[j]) ? 0x7FFFFFFFu : __float_as_uint(f[j]);
+            stg_stream(y + i * 16, make_uint4(o[0], o[1], o[2], o[3]));
         }
     }
 }
@@ -338,7 +338,8 @@ extern "C" fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scale
     const bool bf16 = out_dtype == FP8_DT_BF16;
     if (cols % 32 == 0 && aligned16(q) && aligned16(y)) {
         const int64_t n = rows * cols;
-        const dim3 vg((unsigned)((n / 16 + kThreads * 8 - 1) / (kThreads * 8))), vb(kThreads);
+        const int64_t nitems = n / (bf16 ? 8 : 4);
+        const dim3 vg((unsigned)((nitems + kThreads * 16 - 1) / (kThreads * 16))), vb(kThreads);
         if (fmt == FP8_E4M3)
             return bf16 ? launch(fn, mx_dequant_vec_kernel<kE4M3, true>, vg, vb, st, q, scales, n, yp)
                         : launch(fn, mx_dequant_vec_kernel<kE4M3, false>, vg, vb, st, q, scales, n, yp);

@@ -7,9 +7,9 @@
 // the next scale), §6 (cast_to_fp8 feeding the FP8 GEMM), §24 (overflow counts
 // per layer).
 //
-// HBM-bound: each thread moves 16 elements per unit (two 16-byte BF16 loads or
-// four 16-byte fp32 loads in, one 16-byte code store out) and keeps 8 loads in
-// flight; one CTA per fixed chunk of 16384 (BF16) / 8192 (fp32) elements.
+// HBM-bound: each thread moves items of one 16-byte load (8 BF16 / 4 fp32
+// elements in, 8 / 4 codes out) and keeps 8 loads in flight; one CTA per fixed
+// chunk of 16384 (BF16) / 8192 (fp32) elements.
 // Chunks run in reverse order with evict_first loads: after an amax pass over
 // x (current scaling) the end of x is the part still in L2.  Reductions store
 // one partial per CTA in the stream workspace (plain stores, so a CTA retires
@@ -22,10 +22,14 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Items of one 16-byte load (8 BF16 / 4 fp32 elements -> 8 / 4 codes): a warp
+// loads 512 contiguous bytes and stores 256 / 128 contiguous bytes per item
+// (16-byte loads at a 32- or 64-byte lane stride, each touching half or a
+// quarter of every sector, measured slower); 8 items in flight per thread.
 template <bool BF16> struct VecCfg {
-    static constexpr int kUnits = BF16 ? 4 : 2;
-    static constexpr int kLoads = BF16 ? 2 : 4;  // 16-byte loads per unit
-    static constexpr int64_t kUnitsPerCta = (int64_t)kThreads * kUnits;
+    static constexpr int kPer = BF16 ? 8 : 4;  // elements per item
+    static constexpr int kItems = 8;
+    static constexpr int64_t kItemsPerCta = (int64_t)kThreads * kItems;
 };
 
 // Current scaling inside the cast: the amax kernel left one partial per CTA;
@@ -75,8 +79,8 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
                     uint32_t* __restrict__ part_amax, unsigned long long* __restrict__ part_sat, CurArgs cur) {
     pdl_begin();
     using C = VecCfg<BF16>;
-    const int64_t nunits = n / 16;
-    const int64_t nchunks = (nunits + C::kUnitsPerCta - 1) / C::kUnitsPerCta;
+    const int64_t nitems = n / C::kPer;
+    const int64_t nchunks = (nitems + C::kItemsPerCta - 1) / C::kItemsPerCta;
     const uint64_t pol = l2_policy_evict_first();
     __shared__ uint32_t cur_red[CUR ? 32 : 1];
     float scale = CUR ? 0.0f : *scale_ptr;
@@ -86,15 +90,12 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
     uint32_t sat = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
         const int64_t chunk = nchunks - 1 - c;  // reverse order
-        const int64_t ubase = chunk * C::kUnitsPerCta + threadIdx.x;
-        uint4 v[C::kUnits][C::kLoads];
+        const int64_t ibase = chunk * C::kItemsPerCta + threadIdx.x;
+        uint4 v[C::kItems];
 #pragma unroll
-        for (int k = 0; k < C::kUnits; ++k) {
-            const int64_t u = ubase + (int64_t)k * kThreads;
-            if (u < nunits) {
-#pragma unroll
-                for (int h = 0; h < C::kLoads; ++h) v[k][h] = ldg_stream_hint(x + u * (BF16 ? 32 : 64) + h * 16, pol);
-            }
+        for (int k = 0; k < C::kItems; ++k) {
+            const int64_t i = ibase + (int64_t)k * kThreads;
+            if (i < nitems) v[k] = ldg_stream_hint(x + i * 16, pol);
         }
         if constexpr (CUR) {
             if (!have_scale) {  // the loads above are in flight meanwhile
@@ -103,32 +104,23 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
             }
         }
 #pragma unroll
-        for (int k = 0; k < C::kUnits; ++k) {
-            const int64_t u = ubase + (int64_t)k * kThreads;
-            if (u >= nunits) break;
+        for (int k = 0; k < C::kItems; ++k) {
+            const int64_t i = ibase + (int64_t)k * kThreads;
+            if (i >= nitems) break;
             if constexpr (BF16) {
-                Codes8 cd[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t m;
-                    cd[h] = cvt_bf16x8<FMT>(v[k][h], scale, &m);
-                    if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale))
-                        sat += fixup_bf16x8<FMT>(v[k][h], scale, &cd[h]);
-                    if constexpr (AMAX) am16 = max_u16x2(am16, m);
-                }
-                stg_stream(q + u * 16, make_uint4(cd[0].lo, cd[0].hi, cd[1].lo, cd[1].hi));
+                uint32_t m;
+                Codes8 cd = cvt_bf16x8<FMT>(v[k], scale, &m);
+                if (chunk_needs_fixup<FMT, SAT>(fold_u16x2_to_f32bits(m), scale)) sat += fixup_bf16x8<FMT>(v[k], scale, &cd);
+                if constexpr (AMAX) am16 = max_u16x2(am16, m);
+                stg_stream(q + i * 8, make_uint2(cd.lo, cd.hi));
             } else {
-                uint32_t w[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float4 f = make_float4(__uint_as_float(v[k][h].x), __uint_as_float(v[k][h].y),
-                                           __uint_as_float(v[k][h].z), __uint_as_float(v[k][h].w));
-                    uint32_t m;
-                    w[h] = cvt_f32x4<FMT>(f, scale, &m);
-                    if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w[h]);
-                    if constexpr (AMAX) am32 = umax(am32, m);
-                }
-                stg_stream(q + u * 16, make_uint4(w[0], w[1], w[2], w[3]));
+                const float4 f = make_float4(__uint_as_float(v[k].x), __uint_as_float(v[k].y), __uint_as_float(v[k].z),
+                                             __uint_as_float(v[k].w));
+                uint32_t m;
+                uint32_t w = cvt_f32x4<FMT>(f, scale, &m);
+                if (chunk_needs_fixup<FMT, SAT>(m, scale)) sat += fixup_f32x4<FMT>(f, scale, &w);
+                if constexpr (AMAX) am32 = umax(am32, m);
+                __stcs(reinterpret_cast<unsigned int*>(q + i * 4), w);
             }
         }
     }
@@ -136,9 +128,9 @@ quantize_vec_kernel(const uint8_t* __restrict__ x, uint8_t* __restrict__ q, int6
     if constexpr (CUR) {
         if (!have_scale) scale = scale_from_partials<FMT>(cur, cur_red);  // a CTA without chunks (tiny n)
     }
-    // Tail (< 16 elements): CTA 0.
+    // Tail (< one item): CTA 0.
     if (blockIdx.x == 0) {
-        for (int64_t i = nunits * 16 + threadIdx.x; i < n; i += kThreads) {
+        for (int64_t i = nitems * C::kPer + threadIdx.x; i < n; i += kThreads) {
             float xv;
             uint32_t b;
             if constexpr (BF16) {
@@ -225,8 +217,8 @@ fp8_status_t enqueue_cast(const uint8_t* x, bool bf16, int64_t n, int fmt, const
     uint32_t* pa = reduce ? ws->amax : nullptr;
     unsigned long long* ps = reduce ? ws->sat : nullptr;
     if (aligned16(x) && aligned16(q)) {
-        const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
-        int64_t grid = (n / 16 + per_cta - 1) / per_cta;
+        const int64_t per_cta = bf16 ? VecCfg<true>::kItemsPerCta : VecCfg<false>::kItemsPerCta;
+        int64_t grid = (n / (bf16 ? 8 : 4) + per_cta - 1) / per_cta;
         const int64_t cap = reduce ? kMaxPartials : 0x7FFFFFFF;
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
@@ -387,8 +379,8 @@ extern "C" fp8_status_t fp8_quantize_current(const void* x, fp8_dtype_t dtype, i
     cur.amax_out = amax_out;
     cur.scale_out = scale_out;
     cur.scale_inv_out = scale_inv_out;
-    const int64_t per_cta = bf16 ? VecCfg<true>::kUnitsPerCta : VecCfg<false>::kUnitsPerCta;
-    int64_t grid = (n / 16 + per_cta - 1) / per_cta;
+    const int64_t per_cta = bf16 ? VecCfg<true>::kItemsPerCta : VecCfg<false>::kItemsPerCta;
+    int64_t grid = (n / (bf16 ? 8 : 4) + per_cta - 1) / per_cta;
     if (grid > 0x7FFFFFFF) grid = 0x7FFFFFFF;
     if (grid < 1) grid = 1;
     const uint8_t* xp = static_cast<const uint8_t*>(x);
