@@ -153,6 +153,10 @@ class EventTimer:
         """name -> (total ms, launches); call after a synchronize."""
         return {k: (sum(a.elapsed_time(b) for a, b in v), len(v)) for k, v in self.spans.items()}
 
+    def medians(self):
+        """name -> median ms of one bracketed call; call after a synchronize."""
+        return {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in self.spans.items()}
+
 
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
@@ -333,12 +337,13 @@ def run_ours(args, rank, world):
 
     peak, peak_kind = measured_hbm_peak()
     kernels = {}
+    medians = timer.medians()
     for name, (tot_ms, n) in timer.totals().items():
         nbytes, nl = kb.per_kernel[name]
         gbs = nbytes * ksteps / (tot_ms * 1e-3) / 1e9
         kernels[name] = {"launches_per_step": nl, "bytes_per_step": nbytes, "ms_per_step": round(tot_ms / ksteps, 4),
-                         "avg_launch_us": round(tot_ms * 1e3 / n, 2), "gbs": round(gbs, 1),
-                         "frac": round(gbs / peak, 4)}
+                         "avg_launch_us": round(tot_ms * 1e3 / n, 2), "median_launch_us": round(medians[name] * 1e3, 2),
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
     # The roofline is a single kernel's: the call with the largest share of the
     # step among those that are one kernel launch (the reducing calls add a
     # finalize, fp8_quantize_current is the amax kernel plus the cast).
@@ -349,9 +354,11 @@ def run_ours(args, rank, world):
     for name, (tot_ms, n) in vtimer.totals().items():
         cb = compulsory_bytes({name: pipes[name]})
         gbs = cb * ksteps / (tot_ms * 1e-3) / 1e9
-        variants[name] = {"compulsory_bytes": cb, "kernel_bytes": per_variant_bytes[name].total,
+        kbv = per_variant_bytes[name].total
+        variants[name] = {"compulsory_bytes": cb, "kernel_bytes": kbv,
                           "ms_per_step": round(tot_ms / ksteps, 4), "gbs": round(gbs, 1),
-                          "frac": round(gbs / peak, 4)}
+                          "frac": round(gbs / peak, 4),
+                          "kernel_gbs": round(kbv * ksteps / (tot_ms * 1e-3) / 1e9, 1)}
     traffic_per_elem = kernel_traffic(dominant)
     per_elem_bytes = {"quantize": 3, "quantize_delayed": 3, "cast_transpose": 4, "amax": 2,
                       "dequantize": 3}.get(dominant)

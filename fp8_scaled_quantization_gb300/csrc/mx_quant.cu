@@ -51,15 +51,20 @@ __device__ __forceinline__ uint2 mx_codes8(uint4 v, float m) {
 // Fast path: rows % 32 == 0, cols % 128 == 0, BF16, 16-byte aligned pointers.
 // Load: thread t takes 16 bytes (8 elements) of row t / 16 (+16 on the second
 // pass); the 4 lanes of a 32-element row block reduce its amax by shuffles.
-// The BF16 tile is staged in shared memory (rows padded by 4 bytes) for the
-// columnwise pass, where 2 threads share a column's 32 rows.
+// The BF16 tile is staged in shared memory as 16-byte chunks, chunk k of row r
+// at position k ^ 2 * ((r / 8) % 4): the row stores (8 lanes x 16 bytes) and
+// the column reads below are both free of bank conflicts.  Column pass: thread
+// t owns the column pair 2 * (t / 4), +1 and rows 8 * (t % 4) .. +7; it reads
+// one 32-bit word (two columns) per row, the 4 lanes of a column block combine
+// its amax by shuffles, and each writes 8 codes per column.
+__device__ __forceinline__ int mx_chunk(int row, int chunk) { return chunk ^ (2 * ((row >> 3) & 3)); }
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads)
 mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
     pdl_begin();
-    constexpr int kPad = kTileC + 2;  // row stride in BF16 elements (65 words: conflict-free column reads)
-    __shared__ __align__(16) uint16_t tile[kTileR * kPad];
+    __shared__ __align__(16) uint4 tile[kTileR * kTileC / 8];  // 32 rows x 16 chunks of 8 BF16
     const int64_t gx = cols / kTileC;  // tile (blockIdx.x / gx, blockIdx.x % gx)
     const int64_t r0 = (int64_t)blockIdx.x / gx * kTileR, c0 = (int64_t)blockIdx.x % gx * kTileC;
     const int t = threadIdx.x, lane = t & 31;
@@ -71,11 +76,47 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int r = p * 16 + rsub;
-        uint32_t m16 = max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
-                                 max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w)));
-        uint32_t bits = fold_u16x2_to_f32bits(m16);
+        if (q_row) {
+            uint32_t m16 = max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
+                                     max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w)));
+            uint32_t bits = fold_u16x2_to_f32bits(m16);
+            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
+            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // 4 lanes = one 32-element block
+            uint2 codes;
+            uint32_t code;
+            if (bits >= 0x7F800000u) {
+                code = 0xFFu;
+                codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            } else {
+                code = mx_scale_code<FMT>(bits);
+                codes = mx_codes8<FMT>(v[p], mx_multiplier(code));
+            }
+            stg_stream(q_row + (r0 + r) * cols + c0 + cc * 8, codes);
+            if ((lane & 3) == 0) s_row[(r0 + r) * nbr + (c0 >> 5) + (cc >> 2)] = (uint8_t)code;
+        }
+        if (q_col) tile[r * 16 + mx_chunk(r, cc)] = v[p];
+    }
+    if (!q_col) return;
+    __syncthreads();
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
+    const int cp = t >> 2, g = t & 3;  // columns 2cp, 2cp + 1; rows 8g .. 8g + 7
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = g * 8 + i;
+        w[i] = tw[row * 64 + mx_chunk(row, cp >> 2) * 4 + (cp & 3)];
+    }
+    const int64_t ncb = rows / 32;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t sel = j ? 0x7632u : 0x5410u;  // high or low halves: column 2cp + j
+        const uint4 col = make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
+                                     __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel));
+        uint32_t bits = fold_u16x2_to_f32bits(max_u16x2(max_u16x2(abs_bf16x2(col.x), abs_bf16x2(col.y)),
+                                                        max_u16x2(abs_bf16x2(col.z), abs_bf16x2(col.w))));
         bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
-        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // 4 lanes = one 32-element block
+        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // the 4 row groups of the column block
+        const int64_t c = c0 + 2 * cp + j;
         uint2 codes;
         uint32_t code;
         if (bits >= 0x7F800000u) {
@@ -83,48 +124,11 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
             codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
             code = mx_scale_code<FMT>(bits);
-            codes = mx_codes8<FMT>(v[p], mx_multiplier(code));
+            codes = mx_codes8<FMT>(col, mx_multiplier(code));
         }
-        if (q_row) {
-            stg_stream(q_row + (r0 + r) * cols + c0 + cc * 8, codes);
-            if ((lane & 3) == 0) s_row[(r0 + r) * nbr + (c0 >> 5) + (cc >> 2)] = (uint8_t)code;
-        }
-        if (q_col) {
-            uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[r * kPad + cc * 8]);  // 4-byte aligned (kPad even)
-            dst[0] = v[p].x;
-            dst[1] = v[p].y;
-            dst[2] = v[p].z;
-            dst[3] = v[p].w;
-        }
+        stg_stream(q_col + c * rows + r0 + g * 8, codes);
+        if (g == 0) s_col[c * ncb + (r0 >> 5)] = (uint8_t)code;
     }
-    if (!q_col) return;
-    __syncthreads();
-    // Column pass: thread t owns column c = t / 2, rows 16 * (t % 2) .. +15.
-    const int c = t >> 1, h = t & 1;
-    uint32_t hv[8];  // 16 BF16 values of this thread, as pairs
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = tile[(h * 16 + 2 * i) * kPad + c], b = tile[(h * 16 + 2 * i + 1) * kPad + c];
-        hv[i] = a | (b << 16);
-        m = max_u16x2(m, abs_bf16x2(hv[i]));
-    }
-    uint32_t bits = fold_u16x2_to_f32bits(m);
-    bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));  // the two halves of the column block
-    uint4 out;
-    uint32_t code;
-    if (bits >= 0x7F800000u) {
-        code = 0xFFu;
-        out = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    } else {
-        code = mx_scale_code<FMT>(bits);
-        const float mul = mx_multiplier(code);
-        const uint2 lo = mx_codes8<FMT>(make_uint4(hv[0], hv[1], hv[2], hv[3]), mul);
-        const uint2 hi = mx_codes8<FMT>(make_uint4(hv[4], hv[5], hv[6], hv[7]), mul);
-        out = make_uint4(lo.x, lo.y, hi.x, hi.y);
-    }
-    stg_stream(q_col + (c0 + c) * rows + r0 + h * 16, out);
-    if (h == 0) s_col[(c0 + c) * (rows / 32) + (r0 >> 5)] = (uint8_t)code;
 }
 
 // Guarded path for any shape / dtype / alignment: one thread per block.
