@@ -709,6 +709,7 @@ def cpu_threads():
 
 
 def cpu_baseline(args, inp):
+    import numpy as np
     import oracle as O
     O.build()
     sample = host_sample(inp, args.cpu_fraction, max_w3=len(inp["w3"]), max_w5=len(inp["w5"]))
@@ -722,8 +723,16 @@ def cpu_baseline(args, inp):
     s1, _ = O.compute_scale(O.amax(x1, 1), O.E4M3, 0)
     O.quantize(x1, O.E4M3, s1, 1)
     dt1 = time.perf_counter() - t1
+    # single-threaded: one W5 tensor (amax, scale, quantize, dequantize)
+    x5 = sample["w5"][0]
+    t5 = time.perf_counter()
+    s5, si5 = O.compute_scale(O.amax(x5, 1), O.E5M2, 0)
+    q5, _ = O.quantize(x5, O.E5M2, s5, 1)
+    O.dequantize(q5, O.E5M2, np.array([si5], np.float32), threads=1)
+    dt5 = time.perf_counter() - t5
     return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds": round(dt, 2), "single_thread_w1_gbs": round(x1.size * 5 / dt1 / 1e9, 3),
+            "single_thread_w5_tensor_gbs": round(x5.size * 8 / dt5 / 1e9, 3),
             "sample": f"leading {args.cpu_fraction:.4g} of the rows of every tensor of W1-W5 (all 16 W3 steps, "
                       f"all 32 W5 tensors), one pass; the oracle's own algorithmic bytes ({nbytes / 1e9:.2f} GB)"}
 
