@@ -22,7 +22,9 @@ namespace fp8q {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileR = 32, kTileC = 128;  // 32 x 128 tile: 4 row blocks per row, 1 column block per column
+// 128 x 128 tile of up to four 32-row sub-tiles (the fast path needs rows % 32
+// == 0): 4 row blocks per row and up to 4 column blocks per column.
+constexpr int kTileR = 128, kTileC = 128, kSubR = 32;
 
 template <int FMT> struct MxEmax;
 template <> struct MxEmax<kE4M3> { static constexpr int kE = 8; };
@@ -49,32 +51,52 @@ __device__ __forceinline__ uint2 mx_codes8(uint4 v, float m) {
 }
 
 // Fast path: rows % 32 == 0, cols % 128 == 0, BF16, 16-byte aligned pointers.
-// Load: thread t takes 16 bytes (8 elements) of row t / 16 (+16 on the second
-// pass); the 4 lanes of a 32-element row block reduce its amax by shuffles.
-// The BF16 tile is staged in shared memory as 16-byte chunks, chunk k of row r
-// at position k ^ 2 * ((r / 8) % 4): the row stores (8 lanes x 16 bytes) and
-// the column reads below are both free of bank conflicts.  Column pass: thread
-// t owns the column pair 2 * (t / 4), +1 and rows 8 * (t % 4) .. +7; it reads
-// one 32-bit word (two columns) per row, the 4 lanes of a column block combine
-// its amax by shuffles, and each writes 8 codes per column.
-__device__ __forceinline__ int mx_chunk(int row, int chunk) { return chunk ^ (2 * ((row >> 3) & 3)); }
+// Row pass: thread t takes 16 bytes (8 elements) of rows t / 16 + 16 p, p = 0..7
+// (the sub-tiles inside the tensor); the 4 lanes of a 32-element row block
+// reduce its amax by shuffles.  The BF16 tile is staged in shared memory as
+// 16-byte chunks, chunk k of row r at position k ^ ((r / 16) % 8), so that the
+// row stores (8 lanes x 16 bytes of one row) and the column reads (8 lanes on 8
+// row groups, same chunk) both hit 32 distinct banks.  Column pass: a thread
+// owns the column pair 2 cp, +1 and the 16 rows 16 g .. +15 (twice, cp and
+// cp + 32); it reads one 32-bit word (two columns) per row, lanes g and g ^ 1
+// hold the two halves of a 32-row column block and combine its amax with one
+// shuffle, and each lane stores 16 codes per column: 8 lanes write a column's
+// 128 contiguous bytes, as the cast-transpose does.
+__device__ __forceinline__ int mx_chunk(int row, int chunk) { return chunk ^ ((row >> 4) & 7); }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void mx_block_codes(uint32_t bits, uint4 lo, uint4 hi, uint4* codes, uint32_t* code) {
+    if (bits >= 0x7F800000u) {
+        *code = 0xFFu;
+        *codes = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    } else {
+        *code = mx_scale_code<FMT>(bits);
+        const float m = mx_multiplier(*code);
+        const uint2 a = mx_codes8<FMT>(lo, m), b = mx_codes8<FMT>(hi, m);
+        *codes = make_uint4(a.x, a.y, b.x, b.y);
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 4)
 mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
     pdl_begin();
-    __shared__ __align__(16) uint4 tile[kTileR * kTileC / 8];  // 32 rows x 16 chunks of 8 BF16
+    constexpr int kLoads = kTileR / 16;
+    __shared__ __align__(16) uint4 tile[kTileR * kTileC / 8];  // 128 rows x 16 chunks of 8 BF16
     const int64_t gx = cols / kTileC;  // tile (blockIdx.x / gx, blockIdx.x % gx)
     const int64_t r0 = (int64_t)blockIdx.x / gx * kTileR, c0 = (int64_t)blockIdx.x % gx * kTileC;
+    const int vrows = (int)min((int64_t)kTileR, rows - r0);  // a multiple of 32
     const int t = threadIdx.x, lane = t & 31;
     const int cc = t & 15, rsub = t >> 4;  // 16 threads per 256-byte row
-    uint4 v[2];
+    uint4 v[kLoads];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) v[p] = ldg_stream(x + ((r0 + p * 16 + rsub) * cols + c0 + cc * 8) * 2);
+    for (int p = 0; p < kLoads; ++p)
+        if (p * 16 < vrows) v[p] = ldg_stream(x + ((r0 + p * 16 + rsub) * cols + c0 + cc * 8) * 2);
     const int64_t nbr = cols / 32;
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
+    for (int p = 0; p < kLoads; ++p) {
+        if (p * 16 >= vrows) break;  // uniform over the CTA
         const int r = p * 16 + rsub;
         if (q_row) {
             uint32_t m16 = max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
@@ -99,35 +121,40 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
     if (!q_col) return;
     __syncthreads();
     const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-    const int cp = t >> 2, g = t & 3;  // columns 2cp, 2cp + 1; rows 8g .. 8g + 7
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = g * 8 + i;
-        w[i] = tw[row * 64 + mx_chunk(row, cp >> 2) * 4 + (cp & 3)];
-    }
+    const int g = t & 7;  // rows 16 g .. 16 g + 15
+    const bool live = g * 16 < vrows;  // lanes g and g ^ 1 agree (vrows % 32 == 0)
     const int64_t ncb = rows / 32;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const uint32_t sel = j ? 0x7632u : 0x5410u;  // high or low halves: column 2cp + j
-        const uint4 col = make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
-                                     __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel));
-        uint32_t bits = fold_u16x2_to_f32bits(max_u16x2(max_u16x2(abs_bf16x2(col.x), abs_bf16x2(col.y)),
-                                                        max_u16x2(abs_bf16x2(col.z), abs_bf16x2(col.w))));
-        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
-        bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // the 4 row groups of the column block
-        const int64_t c = c0 + 2 * cp + j;
-        uint2 codes;
-        uint32_t code;
-        if (bits >= 0x7F800000u) {
-            code = 0xFFu;
-            codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-            code = mx_scale_code<FMT>(bits);
-            codes = mx_codes8<FMT>(col, mx_multiplier(code));
+    for (int u = 0; u < 2; ++u) {
+        const int cp = (t >> 3) + 32 * u;  // columns 2 cp, 2 cp + 1
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int row = g * 16 + i;
+            w[i] = tw[row * 64 + mx_chunk(row, cp >> 2) * 4 + (cp & 3)];
         }
-        stg_stream(q_col + c * rows + r0 + g * 8, codes);
-        if (g == 0) s_col[c * ncb + (r0 >> 5)] = (uint8_t)code;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t sel = j ? 0x7632u : 0x5410u;  // high or low halves: column 2 cp + j
+            const uint4 lo = make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
+                                        __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel));
+            const uint4 hi = make_uint4(__byte_perm(w[8], w[9], sel), __byte_perm(w[10], w[11], sel),
+                                        __byte_perm(w[12], w[13], sel), __byte_perm(w[14], w[15], sel));
+            const uint32_t m16 = max_u16x2(max_u16x2(max_u16x2(abs_bf16x2(lo.x), abs_bf16x2(lo.y)),
+                                                     max_u16x2(abs_bf16x2(lo.z), abs_bf16x2(lo.w))),
+                                           max_u16x2(max_u16x2(abs_bf16x2(hi.x), abs_bf16x2(hi.y)),
+                                                     max_u16x2(abs_bf16x2(hi.z), abs_bf16x2(hi.w))));
+            uint32_t bits = fold_u16x2_to_f32bits(m16);
+            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));  // the other half of the 32-row block
+            uint4 codes;
+            uint32_t code;
+            mx_block_codes<FMT>(bits, lo, hi, &codes, &code);
+            const int64_t c = c0 + 2 * cp + j;
+            if (live) {
+                stg_stream(q_col + c * rows + r0 + g * 16, codes);
+                if ((g & 1) == 0) s_col[c * ncb + ((r0 + g * 16) >> 5)] = (uint8_t)code;
+            }
+        }
     }
 }
 
@@ -270,11 +297,11 @@ template <int FMT>
 fp8_status_t launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, uint8_t* q_row, uint8_t* s_row,
                        uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
     const char* w = "fp8_quantize_mx";
-    const bool fast = bf16 && rows % kTileR == 0 && cols % kTileC == 0 && aligned16(x) &&
+    const bool fast = bf16 && rows % kSubR == 0 && cols % kTileC == 0 && aligned16(x) &&
                       (!q_row || aligned16(q_row)) && (!q_col || aligned16(q_col)) &&
-                      (rows / kTileR) * (cols / kTileC) <= 0x7FFFFFFF;
+                      ((rows + kTileR - 1) / kTileR) * (cols / kTileC) <= 0x7FFFFFFF;
     if (fast) {
-        const dim3 grid((unsigned)((rows / kTileR) * (cols / kTileC)));
+        const dim3 grid((unsigned)(((rows + kTileR - 1) / kTileR) * (cols / kTileC)));
         return launch(w, mx_tile_kernel<FMT>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col, s_col);
     }
     const int64_t cap = (int64_t)sm_count() * 8;

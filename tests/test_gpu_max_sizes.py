@@ -119,17 +119,22 @@ def test_blockwise_beyond_2_pow_31(cuda, oracle):
 
 def test_tall_tensors_past_65535_row_tiles(cuda, oracle):
     """Shapes with more than 65535 rows of tiles (the kernels index tiles
-    linearly): MXFP8 (32-row tiles), 128 x 128 blocks and the blockwise
-    cast-transpose (128-row tiles); the last rows against the oracle."""
-    rows = 65536 * 32 + 128  # 2,097,280 rows of MX tiles
+    linearly): MXFP8, 128 x 128 blocks and the blockwise cast-transpose (all
+    128-row tiles); the last rows against the oracle."""
+    rows = 65536 * 128 + 160  # 65538 rows of MX tiles, the last one 32 rows high
     x = big_bf16((rows, 128), 74, cuda)
     q = torch.empty((rows, 128), dtype=torch.uint8, device=cuda)
     s = torch.empty((rows, 4), dtype=torch.uint8, device=cuda)
-    fq.fp8_quantize_mx(x, E4M3, q, s)
+    qc = torch.empty((128, rows), dtype=torch.uint8, device=cuda)
+    sc = torch.empty((128, rows // 32), dtype=torch.uint8, device=cuda)
+    fq.fp8_quantize_mx(x, E4M3, q, s, qc, sc)
     torch.cuda.synchronize()
-    wq, ws = oracle.quantize_mx(host_bits(x[-256:]), E4M3)
+    tail = host_bits(x[-256:])
+    wq, ws = oracle.quantize_mx(tail, E4M3)
     assert np.array_equal(q[-256:].cpu().numpy(), wq) and np.array_equal(s[-256:].cpu().numpy(), ws)
-    del x, q, s
+    wq, ws = oracle.quantize_mx(np.ascontiguousarray(tail.T), E4M3)
+    assert np.array_equal(qc[:, -256:].cpu().numpy(), wq) and np.array_equal(sc[:, -8:].cpu().numpy(), ws)
+    del x, q, s, qc, sc
     rows = 65536 * 128 + 256  # 8,388,864 rows: 65538 row blocks of 128
     x = big_bf16((rows, 128), 75, cuda)
     tail = host_bits(x[-256:])

@@ -35,10 +35,11 @@ def mx_input(shape, dtype, seed, dev, specials=True):
     return x.to(dtype).to(dev)
 
 
-# 32-row multiples with 128-column multiples take the 32 x 128-tile kernel,
-# the rest the guarded kernel.
+# 32-row multiples with 128-column multiples take the 128 x 128-tile kernel
+# (its last row of tiles 32, 64, 96 or 128 rows high), the rest the guarded
+# kernel.
 SHAPES = [(32, 128), (64, 384), (96, 256), (33, 130), (1, 31), (100, 64), (7, 1000), (256, 4096), (128, 128),
-          (384, 256)]
+          (384, 256), (160, 256), (224, 128)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
