@@ -421,6 +421,39 @@ def test_cuda_graph_capture_and_replay(cuda, oracle):
         assert np.array_equal(q_row.cpu().numpy(), wr) and np.array_equal(q_col.cpu().numpy(), wc)
 
 
+def test_reducing_casts_in_a_captured_graph(cuda, oracle):
+    """The reducing casts and their finalize replayed from a graph, with the
+    stream workspace created inside the capture."""
+    x = random_input(1_000_000, torch.bfloat16, 71, cuda)
+    one = dev_scalar(np.float32(1.0), cuda)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=cuda)
+    qd = torch.empty(x.shape, dtype=torch.uint8, device=cuda)
+    am = torch.empty(1, device=cuda)
+    sat = torch.empty(1, dtype=torch.int64, device=cuda)
+    hist = torch.zeros(16, device=cuda)
+    s, si = dev_scalar(np.float32(1.0), cuda), dev_scalar(np.float32(1.0), cuda)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fq.fp8_quantize(x, E4M3, one, q, am, sat)
+        fq.fp8_quantize_delayed(x, E4M3, s, si, qd, hist, 3, fq.AMAX_MAX, 0)
+    prev = np.float32(1.0)
+    for _ in range(3):
+        x.mul_(1.5)
+        graph.replay()
+        torch.cuda.synchronize()
+        xb = host_bits(x)
+        wq, wsat = oracle.quantize(xb, E4M3, np.float32(1.0))
+        wam = oracle.amax(xb)
+        assert np.array_equal(q.cpu().numpy(), wq) and sat.item() == wsat
+        assert f32_bits(am.item()) == f32_bits(wam)
+        wqd, _ = oracle.quantize(xb, E4M3, prev)
+        assert np.array_equal(qd.cpu().numpy(), wqd)
+        ws, wsi = oracle.compute_scale(wam, E4M3, 0)  # the other slots hold 0
+        assert f32_bits(s.item()) == f32_bits(ws) and f32_bits(si.item()) == f32_bits(wsi)
+        assert f32_bits(hist[3].item()) == f32_bits(wam)
+        prev = ws
+
+
 def test_launch_counter_counts_kernels(cuda):
     x = random_input(1000, torch.bfloat16, 1, cuda)
     q = torch.empty(1000, dtype=torch.uint8, device=cuda)
