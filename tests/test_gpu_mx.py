@@ -63,6 +63,38 @@ def test_mx_quantize_matches_oracle(cuda, oracle, dtype, fmt, shape):
     assert np.array_equal(q_col.cpu().numpy(), wqt)
 
 
+def test_mx_signed_special_blocks(cuda, oracle):
+    """Blocks of -0.0, all-subnormal blocks of both signs, -Inf among normals,
+    negative NaNs and +-BF16 max with equal magnitudes, in both directions of
+    the 128 x 128-tile kernel."""
+    x = mx_input((64, 256), torch.float32, 17, "cpu", specials=False)
+    v = x.view(-1)
+    v[0:32] = -0.0
+    sub = torch.tensor([1e-39, -2e-39, 5e-40, -9e-41], dtype=torch.float32)
+    v[32:64] = sub.repeat(8)
+    v[64 + 5] = float("-inf")
+    v[96 + 3] = -float("nan")
+    v[128:160] = torch.tensor([3.3895e38, -3.3895e38] * 16)
+    v[160:192] = torch.tensor([-2.0, 2.0] * 16)
+    x[:, 200] = -0.0          # a column of -0.0 (columnwise blocks)
+    x[0:32, 201] = -1e-39     # a columnwise all-subnormal block
+    x[40, 202] = float("-inf")
+    x = x.to(torch.bfloat16).to(cuda)
+    rows, cols = x.shape
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+    s_row = torch.empty((rows, cols // 32), dtype=torch.uint8, device=cuda)
+    q_col = torch.empty((cols, rows), dtype=torch.uint8, device=cuda)
+    s_col = torch.empty((cols, rows // 32), dtype=torch.uint8, device=cuda)
+    for fmt in (E4M3, E5M2):
+        fq.fp8_quantize_mx(x, fmt, q_row, s_row, q_col, s_col)
+        torch.cuda.synchronize()
+        xb = host(x)
+        wq, ws = oracle.quantize_mx(xb, fmt)
+        assert np.array_equal(s_row.cpu().numpy(), ws) and np.array_equal(q_row.cpu().numpy(), wq)
+        wqt, wst = oracle.quantize_mx(np.ascontiguousarray(xb.T), fmt)
+        assert np.array_equal(s_col.cpu().numpy(), wst) and np.array_equal(q_col.cpu().numpy(), wqt)
+
+
 def test_mx_single_direction(cuda, oracle):
     x = mx_input((64, 256), torch.bfloat16, 5, cuda)
     q = torch.empty((256, 64), dtype=torch.uint8, device=cuda)
