@@ -68,6 +68,36 @@ def test_grouped_matches_per_tensor_calls(cuda):
         assert torch.equal(qs[i], q1), i
 
 
+def test_grouped_at_the_128_tensor_limit(cuda, oracle):
+    """The largest group a table takes: 128 tensors of mixed sizes (empty ones
+    included), E5M2, margin 2."""
+    sizes = [(i * 977) % 6001 for i in range(128)]
+    xs = [random_input(n, torch.bfloat16, 900 + i, cuda) for i, n in enumerate(sizes)]
+    am, s, si = (torch.full((128,), -3.0, device=cuda) for _ in range(3))
+    fq.fp8_amax_grouped(xs, am, E5M2, 2, s, si)
+    qs = [torch.empty(x.shape, dtype=torch.uint8, device=cuda) for x in xs]
+    fq.fp8_quantize_grouped(xs, E5M2, s, qs)
+    torch.cuda.synchronize()
+    for i, x in enumerate(xs):
+        xb = host_bits(x)
+        wa = oracle.amax(xb)
+        ws, wsi = oracle.compute_scale(wa, E5M2, 2)
+        assert f32_bits(am[i].item()) == f32_bits(wa), i
+        assert (f32_bits(s[i].item()), f32_bits(si[i].item())) == (f32_bits(ws), f32_bits(wsi)), i
+        wq, _ = oracle.quantize(xb, E5M2, ws)
+        assert np.array_equal(qs[i].cpu().numpy(), wq), i
+
+
+def test_grouped_all_empty(cuda):
+    """A group of empty tensors: amax 0, scale and scale_inv 1, nothing written."""
+    xs = [torch.empty(0, dtype=torch.bfloat16, device=cuda) for _ in range(5)]
+    am, s, si = (torch.full((5,), -3.0, device=cuda) for _ in range(3))
+    fq.fp8_amax_grouped(xs, am, E4M3, 0, s, si)
+    fq.fp8_quantize_grouped(xs, E4M3, s, [torch.empty(0, dtype=torch.uint8, device=cuda) for _ in range(5)])
+    torch.cuda.synchronize()
+    assert am.tolist() == [0.0] * 5 and s.tolist() == [1.0] * 5 and si.tolist() == [1.0] * 5
+
+
 def test_grouped_rejects_bad_tables(cuda):
     base = torch.zeros(1000, dtype=torch.bfloat16, device=cuda)
     am = torch.empty(2, device=cuda)
