@@ -390,14 +390,16 @@ extern "C" fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_
                                                   void* stream) {
     const char* fn = "fp8_block128_scales_to_mx";
     if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative shape", fn);
-    if (rows == 0 || cols == 0) return FP8_OK;
-    if (scale_inv == nullptr || mx_scales == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-    if (reinterpret_cast<uintptr_t>(scale_inv) % 4) return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", fn);
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && (scale_inv == nullptr || mx_scales == nullptr)) return fail(FP8_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if (!empty && reinterpret_cast<uintptr_t>(scale_inv) % 4)
+        return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", fn);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (bad_blocks_out) {
+    if (bad_blocks_out) {  // overwritten, also for an empty shape
         cudaError_t e = cudaMemsetAsync(bad_blocks_out, 0, sizeof(unsigned long long), st);
         if (e != cudaSuccess) return cuda_status(e, "fp8_block128_scales_to_mx: cudaMemsetAsync");
     }
+    if (empty) return FP8_OK;
     int64_t g = (rows * ((cols + 31) / 32) + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)sm_count() * 8;
     g = g < 1 ? 1 : (g > cap ? cap : g);

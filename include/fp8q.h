@@ -400,7 +400,8 @@ fp8_status_t fp8_dequantize_mx(const uint8_t* q, const uint8_t* scales, fp8_form
  * fp8_quantize_block).  A scale_inv that is not a power of two in
  * [2^-127, 2^127] cannot be carried: its blocks get 0xFF and, when
  * bad_blocks_out (device uint64[1]) is given, it receives how many 128 x 128
- * blocks were like that.  One memset node (bad_blocks_out) + one launch. */
+ * blocks were like that (0 for an empty shape, which launches nothing
+ * else).  One memset node (bad_blocks_out) + one launch. */
 fp8_status_t fp8_block128_scales_to_mx(const float* scale_inv, int64_t rows, int64_t cols, uint8_t* mx_scales,
                                        unsigned long long* bad_blocks_out, void* stream);
 

@@ -140,6 +140,14 @@ def test_block128_to_mx_rescale_matches_oracle(cuda, oracle):
     assert bad.item() == wbad >= 2
 
 
+def test_block128_to_mx_empty_shape_clears_the_count(cuda):
+    bad = torch.full((1,), 7, dtype=torch.int64, device=cuda)
+    out = torch.empty((0, 4), dtype=torch.uint8, device=cuda)
+    fq.fp8_block128_scales_to_mx(torch.empty((0, 1), device=cuda), 0, 128, out, bad)
+    torch.cuda.synchronize()
+    assert bad.item() == 0
+
+
 def test_mx_full_size_activation(cuda, oracle):
     x = wl.w2_student_t(device=cuda)  # 8192 x 8192 BF16
     rows, cols = x.shape
