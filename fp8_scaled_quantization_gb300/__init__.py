@@ -30,7 +30,7 @@ __all__ = [
     "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_quantize_mx", "fp8_dequantize_mx",
     "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "fp8_quantize_current", "fp8_quantize_hybrid", "fp8_quantize_block_cast_transpose",
     "fp8_amax_grouped", "fp8_quantize_grouped", "COLUMNWISE_FROM_ORIGINAL", "COLUMNWISE_FROM_ROWWISE_DEQUANTIZED",
-    "launch_count", "version", "library",
+    "launch_count", "version", "library", "release_stream_workspace",
 ]
 
 
@@ -52,6 +52,12 @@ def version() -> int:
 def launch_count() -> int:
     """Kernels launched by the library so far in this process."""
     return int(library().fp8_launch_count())
+
+
+def release_stream_workspace(stream=None):
+    """Free the library's reduction workspace of `stream` (default: the current
+    stream) on the current device, after the stream's queued work."""
+    _check(library().fp8_release_stream_workspace(_stream(stream)))
 
 
 def _check(status: int):

@@ -102,4 +102,23 @@ int fp8_version(void) { return (FP8Q_VERSION_MAJOR << 16) | FP8Q_VERSION_MINOR; 
 
 unsigned long long fp8_launch_count(void) { return fp8q::g_launches.load(std::memory_order_relaxed); }
 
+fp8_status_t fp8_release_stream_workspace(void* stream) {
+    using namespace fp8q;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "fp8_release_stream_workspace: cudaGetDevice");
+    Workspace* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_workspaces.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(stream)));
+        if (it == g_workspaces.end()) return FP8_OK;  // nothing was allocated for this stream
+        ws = it->second;
+        g_workspaces.erase(it);
+    }
+    // The stream's queued work may still use the workspace.
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaFree(ws);
+    return cuda_status(e, "fp8_release_stream_workspace");
+}
+
 }  // extern "C"

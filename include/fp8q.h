@@ -110,6 +110,15 @@ int fp8_version(void);
  * all threads).  Lets a caller count launches inside a timed region. */
 unsigned long long fp8_launch_count(void);
 
+/* Frees the reduction workspace (96 KB) that the calls made on `stream` on the
+ * current device, after waiting for the work queued on that stream.  A later
+ * reducing call on the stream allocates a new one.  Returns FP8_OK when there
+ * is none.  Call it before destroying a stream when many short-lived streams
+ * are used, and not while the stream is being captured or while a captured
+ * graph whose kernels used that workspace may still be launched (its nodes
+ * hold the workspace's address). */
+fp8_status_t fp8_release_stream_workspace(void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* amax reduction with optional fused current-scaling finalize              */
 /* ------------------------------------------------------------------------ */

@@ -401,6 +401,24 @@ def test_two_streams_use_separate_workspaces(cuda, oracle):
         assert (ama.item(), amb.item()) == (float(wa), float(wb))
 
 
+def test_release_stream_workspace_and_reuse(cuda, oracle):
+    """A stream's workspace is freed after its queued work and allocated again
+    by the next reducing call; releasing twice, or a stream that never had
+    one, is a no-op."""
+    x = random_input(3_000_000, torch.bfloat16, 13, cuda)
+    want = float(oracle.amax(host_bits(x)))
+    st = torch.cuda.Stream()
+    fq.release_stream_workspace(torch.cuda.Stream())
+    for _ in range(3):
+        am = torch.empty(1, device=cuda)
+        with torch.cuda.stream(st):
+            fq.fp8_amax(x, am)
+            fq.release_stream_workspace(st)
+            fq.release_stream_workspace(st)
+        st.synchronize()
+        assert am.item() == want
+
+
 def test_cuda_graph_capture_and_replay(cuda, oracle):
     x = random_input((512, 768), torch.bfloat16, 21, cuda)
     am, s, si = (torch.empty(1, device=cuda) for _ in range(3))
