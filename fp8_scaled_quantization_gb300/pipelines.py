@@ -20,8 +20,9 @@ from dataclasses import dataclass, field
 
 import torch
 
-from . import (AMAX_MAX, E4M3, E5M2, fp8_amax, fp8_dequantize, fp8_quantize, fp8_quantize_block,
-               fp8_quantize_cast_transpose, fp8_quantize_current, fp8_quantize_delayed, fp8_update_scale_delayed)
+from . import (AMAX_MAX, E4M3, E5M2, fp8_amax, fp8_amax_grouped, fp8_dequantize, fp8_quantize, fp8_quantize_block,
+               fp8_quantize_cast_transpose, fp8_quantize_current, fp8_quantize_delayed, fp8_quantize_grouped,
+               fp8_update_scale_delayed)
 
 
 def _f32(dev, n=1, fill=None):
@@ -186,22 +187,50 @@ class BlockScaling:
 
 
 class GradientQDQ:
-    """Per tensor: E5M2 current scaling, then dequantize back to BF16."""
+    """Per tensor: E5M2 current scaling, then dequantize back to BF16.
+
+    group="all": the amax, scale and cast of all tensors are two grouped calls
+    (every tensor keeps its own amax and scale; three launches in all), then
+    each tensor is dequantized, last tensor first, so that the codes written
+    last are read while still in L2.  group="amax": one grouped amax + scale
+    call for all tensors, then per tensor the cast and, right after it, the
+    dequantize, which reads the codes while they are still in L2.  Otherwise
+    (group="", and in run_tensor, which the host-buffer path uses one tensor
+    at a time) each tensor is one fp8_quantize_current call (current_call=True)
+    or fp8_amax + fp8_quantize, then its dequantize."""
 
     def __init__(self, xs: list, fmt: int = E5M2, margin: int = 0, keep_outputs: bool = False,
-                 current_call: bool = True):
-        self.xs, self.fmt, self.margin, self.current_call = xs, fmt, margin, current_call
+                 current_call: bool = True, group: str = ""):
+        if group not in ("", "amax", "all"):
+            raise ValueError("group must be '', 'amax' or 'all'")
+        self.xs, self.fmt, self.margin, self.current_call, self.group = xs, fmt, margin, current_call, group
         dev = xs[0].device
-        n = len(xs) if keep_outputs else 1
-        self.q = [torch.empty(xs[0].shape, dtype=torch.uint8, device=dev) for _ in range(n)]
-        self.y = [torch.empty(xs[0].shape, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        nq = len(xs) if (keep_outputs or group == "all") else 1  # the grouped cast writes every tensor's codes
+        ny = len(xs) if keep_outputs else 1
+        self.q = [torch.empty(xs[0].shape, dtype=torch.uint8, device=dev) for _ in range(nq)]
+        self.y = [torch.empty(xs[0].shape, dtype=torch.bfloat16, device=dev) for _ in range(ny)]
         self.amax = torch.empty(len(xs), dtype=torch.float32, device=dev)
         self.scale = torch.empty(len(xs), dtype=torch.float32, device=dev)
         self.scale_inv = torch.empty(len(xs), dtype=torch.float32, device=dev)
 
     def run(self, timer=None):
-        for k in range(len(self.xs)):
-            self.run_tensor(k, timer)
+        if not self.group:
+            for k in range(len(self.xs)):
+                self.run_tensor(k, timer)
+            return
+        _t(timer, "amax_grouped", lambda: fp8_amax_grouped(self.xs, self.amax, self.fmt, self.margin, self.scale,
+                                                           self.scale_inv))
+        if self.group == "amax":
+            for k in range(len(self.xs)):
+                x, q, y = self.xs[k], self.q[k % len(self.q)], self.y[k % len(self.y)]
+                s, si = self.scale[k:k + 1], self.scale_inv[k:k + 1]
+                _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
+                _t(timer, "dequantize", lambda: fp8_dequantize(q, self.fmt, si, y))
+            return
+        _t(timer, "quantize_grouped", lambda: fp8_quantize_grouped(self.xs, self.fmt, self.scale, self.q))
+        for k in reversed(range(len(self.xs))):
+            q, y, si = self.q[k], self.y[k % len(self.y)], self.scale_inv[k:k + 1]
+            _t(timer, "dequantize", lambda: fp8_dequantize(q, self.fmt, si, y))
 
     def run_tensor(self, k: int, timer=None):
         x, q, y = self.xs[k], self.q[k % len(self.q)], self.y[k % len(self.y)]
@@ -216,6 +245,15 @@ class GradientQDQ:
 
     def bytes(self) -> KernelBytes:
         b = KernelBytes()
+        if self.group:
+            b.add("amax_grouped", sum(x.numel() * esize(x) for x in self.xs))
+            if self.group == "all":
+                b.add("quantize_grouped", sum(x.numel() * (esize(x) + 1) for x in self.xs))
+            for x in self.xs:
+                if self.group == "amax":
+                    b.add("quantize", x.numel() * (esize(x) + 1))
+                b.add("dequantize", x.numel() * (1 + 2))
+            return b
         for x in self.xs:
             n = x.numel()
             if self.current_call:

@@ -15,6 +15,11 @@ from fp8_scaled_quantization_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
+def bench_w5_group():
+    import bench
+    return bench.W5_GROUP
+
+
 def bits(x):
     return wl.bf16_bits(x)
 
@@ -103,7 +108,7 @@ def test_w4_blockwise(cuda, oracle, threads):
 
 def test_w5_e5m2_quantize_dequantize(cuda, oracle, threads):
     xs = list(wl.w5_gradients(device=cuda))
-    p = P.GradientQDQ(xs, fq.E5M2, 0, keep_outputs=True)
+    p = P.GradientQDQ(xs, fq.E5M2, 0, keep_outputs=True, group=bench_w5_group())  # as the bench runs it
     p.run()
     torch.cuda.synchronize()
     scales, scale_invs = f32b(p.scale), f32b(p.scale_inv)
@@ -123,3 +128,21 @@ def test_w5_e5m2_quantize_dequantize(cuda, oracle, threads):
             assert np.array_equal(p.q[k][torch.from_numpy(rows).to(cuda)].cpu().numpy(), q)
             y = oracle.dequantize(q, oracle.E5M2, np.array([si]))
             assert np.array_equal(bits(p.y[k][torch.from_numpy(rows).to(cuda)]), y)
+
+
+@pytest.mark.parametrize("group", ["", "amax", "all"])
+def test_w5_pipeline_orders_agree(cuda, oracle, group):
+    """The three ways GradientQDQ can organise the per-tensor current scaling
+    give the same scales, codes and dequantized values (small tensors)."""
+    g = torch.Generator(device="cpu").manual_seed(77)
+    xs = [(torch.randn((257, 384), generator=g) * (10.0 ** k)).to(torch.bfloat16).to(cuda) for k in range(-2, 3)]
+    p = P.GradientQDQ(xs, fq.E5M2, 1, keep_outputs=True, group=group)
+    p.run()
+    torch.cuda.synchronize()
+    for k, x in enumerate(xs):
+        xb = bits(x)
+        s, si = oracle.compute_scale(oracle.amax(xb), oracle.E5M2, 1)
+        assert f32b(p.scale)[k] == s.view(np.uint32) and f32b(p.scale_inv)[k] == si.view(np.uint32), k
+        q, _ = oracle.quantize(xb, oracle.E5M2, s)
+        assert np.array_equal(p.q[k].cpu().numpy(), q), k
+        assert np.array_equal(bits(p.y[k]), oracle.dequantize(q, oracle.E5M2, np.array([si]))), k

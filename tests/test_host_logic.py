@@ -143,8 +143,18 @@ def test_pipeline_byte_accounting_full_size():
     assert b["W5"].total == 32 * 8 * N5
     total = sum(x.total for x in b.values())
     assert 21.0e9 < total < 21.3e9
-    assert b["W5"].per_kernel["quantize_current"] == (32 * 5 * N5, 32)
-    assert sum(x.launches for x in b.values()) == 1 + 2 + (16 + 1) + 2 + 64  # API calls
+    w5 = b["W5"].per_kernel
+    if bench.W5_GROUP == "all":
+        assert w5["amax_grouped"] == (32 * 2 * N5, 1) and w5["quantize_grouped"] == (32 * 3 * N5, 1)
+        w5_calls = 1 + 1 + 32
+    elif bench.W5_GROUP == "amax":
+        assert w5["amax_grouped"] == (32 * 2 * N5, 1) and w5["quantize"] == (32 * 3 * N5, 32)
+        w5_calls = 1 + 32 + 32
+    else:
+        assert w5["quantize_current"] == (32 * 5 * N5, 32)
+        w5_calls = 32 + 32
+    assert w5["dequantize"] == (32 * 3 * N5, 32)
+    assert sum(x.launches for x in b.values()) == 1 + 2 + (16 + 1) + 2 + w5_calls  # API calls
 
 
 # ------------------------------------------------------------- multi-rank
@@ -218,6 +228,8 @@ def test_two_call_current_scaling_byte_accounting():
     assert b.per_kernel == {"amax": (2 * 2 ** 20, 1), "quantize": (3 * 2 ** 20, 1)}
     g = P.GradientQDQ([x, x], current_call=False).bytes()
     assert g.per_kernel["amax"] == (2 * 2 * 2 ** 20, 2) and g.per_kernel["dequantize"] == (2 * 3 * 2 ** 20, 2)
+    c = P.GradientQDQ([x, x]).bytes()
+    assert c.per_kernel["quantize_current"] == (2 * 5 * 2 ** 20, 2)
 
 
 def test_input_digests_hash_each_workloads_bytes():
