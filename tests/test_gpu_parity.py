@@ -382,6 +382,79 @@ def test_delayed_nan_history(cuda):
 
 # ----------------------------------------------- streams, graphs, workspace
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_delayed_history_at_its_limit(cuda, oracle, fused):
+    """A 65536-entry history (the largest accepted) prefilled with amaxes, and
+    step numbers past 2^40, so the slot is a 64-bit remainder and the window
+    maximum runs over every entry but the slot."""
+    L = 65536
+    g = torch.Generator(device="cpu").manual_seed(41)
+    h0 = (torch.rand(L, generator=g) * 300).float()
+    h0[12345] = 2500.0  # the window maximum, until its slot is overwritten
+    hist, h_ref = h0.to(cuda), h0.numpy().copy()
+    s, si = dev_scalar(np.float32(1.0), cuda), dev_scalar(np.float32(1.0), cuda)
+    ws = np.float32(1.0)
+    base = (1 << 40) + 12345 - 2 - ((1 << 40) % L)  # slots 12343, 12344, 12345, 12346
+    for i, k in enumerate(range(base, base + 4)):
+        x = random_input((64, 96), torch.bfloat16, 300 + i, cuda, spread=False)  # amax ~160 < the history's
+        xb = host_bits(x)
+        a = oracle.amax(xb)
+        if fused:
+            q = torch.empty(x.shape, dtype=torch.uint8, device=cuda)
+            fq.fp8_quantize_delayed(x, E4M3, s, si, q, hist, k, fq.AMAX_MAX, 0)
+        else:
+            am = dev_scalar(a, cuda)
+            fq.fp8_update_scale_delayed(hist, k, am, fq.AMAX_MAX, E4M3, 0, s, si)
+        torch.cuda.synchronize()
+        if fused:
+            wq, _ = oracle.quantize(xb, E4M3, ws)
+            assert np.array_equal(q.cpu().numpy(), wq), k
+        ws, wsi = oracle.update_delayed(h_ref, k, a, fq.AMAX_MAX, E4M3, 0)
+        assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi)), k
+        assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32)), k
+
+
+def test_concurrent_host_threads_on_their_own_streams(cuda, oracle):
+    """Four host threads, each with its own stream (and so its own workspace),
+    call the library at the same time; ctypes drops the interpreter lock
+    during the calls, so the workspace table and the error text are used
+    concurrently."""
+    import threading
+    xs = [random_input(2_000_000, torch.bfloat16, 50 + i, cuda) * (i + 1) for i in range(4)]
+    want = [oracle.amax(host_bits(x)) for x in xs]
+    scales = [oracle.compute_scale(w, E4M3, 0)[0] for w in want]
+    codes = [oracle.quantize(host_bits(x), E4M3, sc)[0] for x, sc in zip(xs, scales)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(10):
+                    am, s, si = (torch.empty(1, device=cuda) for _ in range(3))
+                    q = torch.empty(xs[i].shape, dtype=torch.uint8, device=cuda)
+                    fq.fp8_amax(xs[i], am, E4M3, 0, s, si)
+                    fq.fp8_quantize(xs[i], E4M3, s, q)
+                    st.synchronize()
+                    assert f32_bits(am.item()) == f32_bits(want[i]) and np.array_equal(q.cpu().numpy(), codes[i])
+                    try:  # a 2 x 64 block is rejected in the library: this thread's error text
+                        fq.fp8_quantize_block(xs[i][:256].view(2, 128), 2, 64, E4M3, q[:256].view(2, 128),
+                                              torch.empty((1, 2), device=cuda))
+                        raise AssertionError("a 2 x 64 block was accepted")
+                    except fq.Fp8Error as e:
+                        assert e.status == 2 and "block" in str(e), str(e)
+        except Exception as e:  # noqa: BLE001 -- reported below
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+
+
 def test_two_streams_use_separate_workspaces(cuda, oracle):
     xa = random_input(3_000_000, torch.bfloat16, 11, cuda)
     xb = random_input(3_000_000, torch.bfloat16, 12, cuda) * 3
