@@ -15,6 +15,8 @@
 // the NaN scale 0xFF and NaN codes.  floor(log2(amax)) is the exponent field
 // of the fp32 amax, so no division is needed; codes are
 // cvt.rn.satfinite(fl32(x * 2^-shared_exp)).
+#include <type_traits>
+
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -77,10 +79,13 @@ __device__ __forceinline__ void mx_block_codes(uint32_t bits, uint4 lo, uint4 hi
     }
 }
 
-template <int FMT>
+// NARROW (rows, cols < 2^24): addresses are per-tile 64-bit bases plus 32-bit
+// offsets inside the tile, which saves the 64-bit multiply-adds of every access.
+template <int FMT, bool NARROW>
 __global__ void __launch_bounds__(kThreads, 4)
 mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+    using Off = typename std::conditional<NARROW, uint32_t, int64_t>::type;
     pdl_begin();
     constexpr int kLoads = kTileR / 16;
     __shared__ __align__(16) uint4 tile[kTileR * kTileC / 8];  // 128 rows x 16 chunks of 8 BF16
@@ -89,11 +94,17 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
     const int vrows = (int)min((int64_t)kTileR, rows - r0);  // a multiple of 32
     const int t = threadIdx.x, lane = t & 31;
     const int cc = t & 15, rsub = t >> 4;  // 16 threads per 256-byte row
+    const Off ocols = (Off)cols, orows = (Off)rows;
+    const Off nbr = (Off)(cols / 32), ncb = (Off)(rows / 32);
+    const uint8_t* xt = x + (r0 * cols + c0) * 2;  // this tile's corner in each array
+    uint8_t* qr = q_row ? q_row + r0 * cols + c0 : nullptr;
+    uint8_t* sr = s_row ? s_row + r0 * (cols / 32) + (c0 >> 5) : nullptr;
+    uint8_t* qc = q_col ? q_col + c0 * rows + r0 : nullptr;
+    uint8_t* sc = s_col ? s_col + c0 * (rows / 32) + (r0 >> 5) : nullptr;
     uint4 v[kLoads];
 #pragma unroll
     for (int p = 0; p < kLoads; ++p)
-        if (p * 16 < vrows) v[p] = ldg_stream(x + ((r0 + p * 16 + rsub) * cols + c0 + cc * 8) * 2);
-    const int64_t nbr = cols / 32;
+        if (p * 16 < vrows) v[p] = ldg_stream(xt + ((Off)(p * 16 + rsub) * ocols + (Off)(cc * 8)) * 2);
 #pragma unroll
     for (int p = 0; p < kLoads; ++p) {
         if (p * 16 >= vrows) break;  // uniform over the CTA
@@ -113,8 +124,8 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
                 code = mx_scale_code<FMT>(bits);
                 codes = mx_codes8<FMT>(v[p], mx_multiplier(code));
             }
-            stg_stream(q_row + (r0 + r) * cols + c0 + cc * 8, codes);
-            if ((lane & 3) == 0) s_row[(r0 + r) * nbr + (c0 >> 5) + (cc >> 2)] = (uint8_t)code;
+            stg_stream(qr + ((Off)r * ocols + (Off)(cc * 8)), codes);
+            if ((lane & 3) == 0) sr[(Off)r * nbr + (Off)(cc >> 2)] = (uint8_t)code;
         }
         if (q_col) tile[r * 16 + mx_chunk(r, cc)] = v[p];
     }
@@ -123,7 +134,6 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
     const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
     const int g = t & 7;  // rows 16 g .. 16 g + 15
     const bool live = g * 16 < vrows;  // lanes g and g ^ 1 agree (vrows % 32 == 0)
-    const int64_t ncb = rows / 32;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int cp = (t >> 3) + 32 * u;  // columns 2 cp, 2 cp + 1
@@ -149,10 +159,10 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
             uint4 codes;
             uint32_t code;
             mx_block_codes<FMT>(bits, lo, hi, &codes, &code);
-            const int64_t c = c0 + 2 * cp + j;
+            const Off c = (Off)(2 * cp + j);  // column inside the tile
             if (live) {
-                stg_stream(q_col + c * rows + r0 + g * 16, codes);
-                if ((g & 1) == 0) s_col[c * ncb + ((r0 + g * 16) >> 5)] = (uint8_t)code;
+                stg_stream(qc + (c * orows + (Off)(g * 16)), codes);
+                if ((g & 1) == 0) sc[c * ncb + (Off)(g >> 1)] = (uint8_t)code;
             }
         }
     }
@@ -302,7 +312,11 @@ fp8_status_t launch_mx(const uint8_t* x, bool bf16, int64_t rows, int64_t cols, 
                       ((rows + kTileR - 1) / kTileR) * (cols / kTileC) <= 0x7FFFFFFF;
     if (fast) {
         const dim3 grid((unsigned)(((rows + kTileR - 1) / kTileR) * (cols / kTileC)));
-        return launch(w, mx_tile_kernel<FMT>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col, s_col);
+        if (rows < (1 << 24) && cols < (1 << 24))
+            return launch(w, mx_tile_kernel<FMT, true>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col,
+                          s_col);
+        return launch(w, mx_tile_kernel<FMT, false>, grid, dim3(kThreads), st, x, rows, cols, q_row, s_row, q_col,
+                      s_col);
     }
     const int64_t cap = (int64_t)sm_count() * 8;
     if (q_row) {
