@@ -137,12 +137,11 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int cp = (t >> 3) + 32 * u;  // columns 2 cp, 2 cp + 1
+        // rows 16 g .. 16 g + 15 all have (row / 16) % 8 == g, so one chunk swizzle
+        const uint32_t* wcol = tw + g * 16 * 64 + mx_chunk(g * 16, cp >> 2) * 4 + (cp & 3);
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int row = g * 16 + i;
-            w[i] = tw[row * 64 + mx_chunk(row, cp >> 2) * 4 + (cp & 3)];
-        }
+        for (int i = 0; i < 16; ++i) w[i] = wcol[i * 64];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const uint32_t sel = j ? 0x7632u : 0x5410u;  // high or low halves: column 2 cp + j
