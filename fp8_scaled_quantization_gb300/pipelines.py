@@ -8,11 +8,13 @@ call into the CUDA library.
   CurrentScaling     "Megatron FP8" §4/§10: fp8_quantize_current (amax kernel, then a cast
                      that derives the scale itself), or fp8_amax (+ scale) -> fp8_quantize
   CurrentCastTranspose  same, with rowwise + columnwise outputs (§6)
-  DelayedScaling     §5: per step fp8_quantize (fused amax, saturation count)
-                     -> fp8_update_scale_delayed (history ring, window max)
+  DelayedScaling     §5: per step fp8_quantize_delayed (the cast records amax and the
+                     saturation count; its finalize writes the history ring and the next
+                     scale), or fp8_quantize -> fp8_update_scale_delayed
   BlockScaling       "Low Precision Training and Rollout": fp8_quantize_block
                      128 x 128 (weight) and 1 x 128 (activation)
-  GradientQDQ        E5M2 current scaling then fp8_dequantize back to BF16
+  GradientQDQ        E5M2 current scaling then fp8_dequantize back to BF16, per tensor or
+                     with one grouped amax + scale call over all tensors (§21)
 """
 from __future__ import annotations
 
