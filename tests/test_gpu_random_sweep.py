@@ -244,3 +244,68 @@ def test_delayed_sequence(cuda, oracle, case):
         ws, wsi = oracle.update_delayed(h_ref, k, wa, algo, fmt, margin)
         assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi)), k
         assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32)), k
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_grouped(cuda, oracle, case):
+    rng = np.random.default_rng(10000 + case)
+    count = int(rng.choice([1, 2, 5, 33, int(rng.integers(1, 129))]))
+    dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+    fmt = E4M3 if rng.random() < 0.5 else E5M2
+    margin = int(rng.integers(-2, 3))
+    xs = []
+    for _ in range(count):
+        n = int(rng.choice([0, 1, 8, 4096, int(rng.integers(1, 40000))]))
+        x = draw_tensor(rng, (n + 8,), dtype, cuda)  # grouped tensors must be 16-byte aligned:
+        xs.append(x.contiguous()[:n] if x.data_ptr() % 16 == 0 else x.clone()[:n])  # re-based copies
+    am, s, si = (torch.empty(count, device=cuda) for _ in range(3))
+    fq.fp8_amax_grouped(xs, am, fmt, margin, s, si)
+    qs = [torch.empty(x.shape, dtype=torch.uint8, device=cuda) for x in xs]
+    fq.fp8_quantize_grouped(xs, fmt, s, qs)
+    torch.cuda.synchronize()
+    for i, x in enumerate(xs):
+        xb = host_bits(x)
+        wa = oracle.amax(xb)
+        ws, wsi = oracle.compute_scale(wa, fmt, margin)
+        assert f32_bits(am[i].item()) == f32_bits(wa), i
+        assert (f32_bits(s[i].item()), f32_bits(si[i].item())) == (f32_bits(ws), f32_bits(wsi)), i
+        assert np.array_equal(qs[i].cpu().numpy(), oracle.quantize(xb, fmt, ws)[0]), i
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_mx_dequantize(cuda, oracle, case):
+    rng = np.random.default_rng(11000 + case)
+    rows, cols = shape2(rng, 200)
+    if rng.random() < 0.5:
+        cols = 32 * int(rng.integers(1, 8))  # the vector kernel's shapes
+    fmt = E4M3 if rng.random() < 0.5 else E5M2
+    out_bf16 = rng.random() < 0.6
+    g = torch.Generator().manual_seed(11000 + case)
+    q = torch.randint(0, 256, (rows, cols), generator=g, dtype=torch.uint8)
+    sc = torch.randint(0, 256, (rows, -(-cols // 32)), generator=g, dtype=torch.uint8)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=cuda)
+    fq.fp8_dequantize_mx(q.to(cuda), sc.to(cuda), fmt, y)
+    torch.cuda.synchronize()
+    want = oracle.dequantize_mx(q.numpy(), sc.numpy(), fmt, out_dt=oracle.BF16 if out_bf16 else oracle.FP32)
+    got = host_bits(y)
+    if out_bf16:
+        assert np.array_equal(got, want)
+    else:
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_block128_scales_to_mx(cuda, oracle, case):
+    rng = np.random.default_rng(12000 + case)
+    rows, cols = shape2(rng, 700)
+    nbr, nbc = -(-rows // 128), -(-cols // 128)
+    k = rng.integers(-140, 130, size=(nbr, nbc))
+    si = np.ldexp(np.float32(1.0), k).astype(np.float32)
+    odd = rng.random((nbr, nbc)) < 0.1
+    si[odd] = np.float32(3.0)  # not a power of two
+    out = torch.empty((rows, -(-cols // 32)), dtype=torch.uint8, device=cuda)
+    bad = torch.empty(1, dtype=torch.int64, device=cuda)
+    fq.fp8_block128_scales_to_mx(torch.from_numpy(si).to(cuda), rows, cols, out, bad)
+    torch.cuda.synchronize()
+    want, wbad = oracle.block128_scales_to_mx(si, rows, cols)
+    assert np.array_equal(out.cpu().numpy(), want) and bad.item() == wbad
