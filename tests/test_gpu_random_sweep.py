@@ -228,9 +228,10 @@ def test_delayed_sequence(cuda, oracle, case):
     s, si = dev_scalar(np.float32(1.0), cuda), dev_scalar(np.float32(1.0), cuda)
     ws = np.float32(1.0)
     step0 = int(rng.integers(0, 1 << 40))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
     for k in range(step0, step0 + 5):
         n = int(rng.integers(0, 50000))
-        x = draw_tensor(rng, (n,), torch.bfloat16, cuda)
+        x = draw_tensor(rng, (n,), dtype, cuda)
         q = torch.empty(n, dtype=torch.uint8, device=cuda)
         am = torch.empty(1, device=cuda)
         sat = torch.empty(1, dtype=torch.int64, device=cuda)
@@ -309,3 +310,46 @@ def test_block128_scales_to_mx(cuda, oracle, case):
     torch.cuda.synchronize()
     want, wbad = oracle.block128_scales_to_mx(si, rows, cols)
     assert np.array_equal(out.cpu().numpy(), want) and bad.item() == wbad
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_amax_and_scale(cuda, oracle, case):
+    rng = np.random.default_rng(13000 + case)
+    n = int(rng.choice([0, 1, 3, 9, 4096, int(rng.integers(1, 4_000_000))]))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+    fmt = E4M3 if rng.random() < 0.5 else E5M2
+    margin = int(rng.integers(-5, 6))
+    x = draw_tensor(rng, (n,), dtype, cuda)
+    am, s, si = (torch.empty(1, device=cuda) for _ in range(3))
+    if rng.random() < 0.5 and n <= (1 << 28):
+        fq.fp8_amax_noalloc(x, am, fmt, margin, s, si)
+    else:
+        fq.fp8_amax(x, am, fmt, margin, s, si)
+    torch.cuda.synchronize()
+    wa = oracle.amax(host_bits(x))
+    ws, wsi = oracle.compute_scale(wa, fmt, margin)
+    assert f32_bits(am.item()) == f32_bits(wa)
+    assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi))
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_update_scale_delayed(cuda, oracle, case):
+    rng = np.random.default_rng(14000 + case)
+    L = int(rng.choice([1, 2, 31, 32, 33, 1024, 65536, int(rng.integers(1, 70000) % 65536 + 1)]))
+    algo = fq.AMAX_MAX if rng.random() < 0.6 else fq.AMAX_MOST_RECENT
+    fmt = E4M3 if rng.random() < 0.5 else E5M2
+    margin = int(rng.integers(-3, 4))
+    h0 = (rng.random(L) * float(10.0 ** rng.uniform(-3, 3))).astype(np.float32)
+    if rng.random() < 0.2:
+        h0[int(rng.integers(L))] = np.float32("nan")
+    hist, h_ref = torch.from_numpy(h0.copy()).to(cuda), h0.copy()
+    s, si = torch.empty(1, device=cuda), torch.empty(1, device=cuda)
+    for _ in range(4):
+        step = int(rng.integers(0, 1 << 45))
+        new = None if rng.random() < 0.2 else np.float32(10.0 ** rng.uniform(-4, 4))
+        fq.fp8_update_scale_delayed(hist, step, None if new is None else dev_scalar(new, cuda), algo, fmt, margin,
+                                    s, si)
+        torch.cuda.synchronize()
+        ws, wsi = oracle.update_delayed(h_ref, step, new, algo, fmt, margin)
+        assert (f32_bits(s.item()), f32_bits(si.item())) == (f32_bits(ws), f32_bits(wsi)), step
+        assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32)), step
