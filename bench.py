@@ -63,6 +63,8 @@ def parse_args():
                     help="comma-separated subset of W1..W5 (profiling a single workload)")
     ap.add_argument("--count", type=int, default=0,
                     help="cap on W3 steps and W5 tensors (0 = the full 16 / 32; profiling only)")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="an NVTX range around every workload of every step (for a timeline profiler)")
     return ap.parse_args()
 
 
@@ -298,11 +300,15 @@ def run_ours(args, rank, world):
 
     def step(timer=None, vt=None):
         for name, p in pipes.items():
+            if args.nvtx:
+                torch.cuda.nvtx.range_push(name)
             if vt is not None:
                 vt.start(name)
             p.run(timer)
             if vt is not None:
                 vt.stop(name)
+            if args.nvtx:
+                torch.cuda.nvtx.range_pop()
 
     for _ in range(args.warmup):
         step()

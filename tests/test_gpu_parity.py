@@ -414,6 +414,40 @@ def test_delayed_history_at_its_limit(cuda, oracle, fused):
         assert np.array_equal(hist.cpu().numpy().view(np.uint32), h_ref.view(np.uint32)), k
 
 
+def test_delayed_resume_from_a_saved_state(cuda):
+    """Checkpoint / resume: all delayed-scaling state lives in caller buffers,
+    so 8 steps, a host copy of history / scale / scale_inv, a restore into
+    fresh device buffers and steps 8-15 give the codes, scales and history of
+    an uninterrupted 16-step run, bit for bit."""
+    xs = list(wl.w3_steps(shape=(96, 160), steps=16, device=cuda))
+
+    def fresh():
+        return torch.zeros(16, device=cuda), dev_scalar(np.float32(1.0), cuda), dev_scalar(np.float32(1.0), cuda)
+
+    def run(state, steps):
+        hist, s, si = state
+        qs = []
+        for k in steps:
+            q = torch.empty(xs[k].shape, dtype=torch.uint8, device=cuda)
+            fq.fp8_quantize_delayed(xs[k], E4M3, s, si, q, hist, k, fq.AMAX_MAX, 0)
+            qs.append(q)
+        return qs
+
+    whole = fresh()
+    q_whole = run(whole, range(16))
+    first = fresh()
+    q_first = run(first, range(8))
+    saved = [t.cpu() for t in first]  # the checkpoint
+    del first
+    resumed = tuple(t.to(cuda) for t in saved)  # restored into new buffers
+    q_rest = run(resumed, range(8, 16))
+    torch.cuda.synchronize()
+    for k, (a, b) in enumerate(zip(q_whole, q_first + q_rest)):
+        assert torch.equal(a, b), k
+    for a, b in zip(whole, resumed):
+        assert np.array_equal(a.cpu().numpy().view(np.uint32), b.cpu().numpy().view(np.uint32))
+
+
 def test_concurrent_host_threads_on_their_own_streams(cuda, oracle):
     """Four host threads, each with its own stream (and so its own workspace),
     call the library at the same time; ctypes drops the interpreter lock
