@@ -223,7 +223,8 @@ class GradientQDQ:
         _t(timer, "amax_grouped", lambda: fp8_amax_grouped(self.xs, self.amax, self.fmt, self.margin, self.scale,
                                                            self.scale_inv))
         if self.group == "amax":
-            for k in range(len(self.xs)):
+            # last tensor first: the grouped amax read it last, so its tail is still in L2
+            for k in reversed(range(len(self.xs))):
                 x, q, y = self.xs[k], self.q[k % len(self.q)], self.y[k % len(self.y)]
                 s, si = self.scale[k:k + 1], self.scale_inv[k:k + 1]
                 _t(timer, "quantize", lambda: fp8_quantize(x, self.fmt, s, q))
