@@ -808,8 +808,8 @@ def run_reference(args, rank, world):
         nbytes += oracle_suite_sample(sample, 1.0, threads)
     dt = time.perf_counter() - t
     v = round(nbytes / dt / 1e9, 3)
-    desc = ("each step: the oracle on 1/8 of the rows of W2, 4 of 16 W3 steps, W4, 4 of 32 W5 tensors, and "
-            "all of W1 (CPU-generated inputs of the same distributions)")
+    desc = ("each step: the oracle on 1/8 of the rows of W2, of W4, of 4 of the 16 W3 steps and of 4 of the 32 "
+            "W5 tensors, and on all of W1 (CPU-generated inputs of the same distributions)")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
