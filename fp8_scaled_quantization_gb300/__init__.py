@@ -75,16 +75,40 @@ def _dt(t: torch.Tensor) -> int:
 
 
 def _p(t) -> int | None:
-    """Data pointer of an optional contiguous CUDA tensor."""
+    """Data pointer of an optional contiguous tensor on the current CUDA device
+    (the library launches on the current device's stream, so a tensor on
+    another device would be reached through a peer pointer)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"expected a tensor, got {type(t)}")
     if not t.is_cuda:
         raise ValueError("tensors passed to the FP8 library must live on a CUDA device")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current CUDA device is cuda:{torch.cuda.current_device()}; "
+                         "call inside `with torch.cuda.device(...)`")
     if not t.is_contiguous():
         raise ValueError("tensors passed to the FP8 library must be contiguous")
     return t.data_ptr() or None
+
+
+def _f32(t, name: str) -> int | None:
+    """Pointer of an optional fp32 device scalar (amax, scale, scale_inv): the
+    library reads or writes one 4-byte word there."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() < 1:
+        raise ValueError(f"{name} must be a float32 tensor of at least one element")
+    return _p(t)
+
+
+def _u64(t, name: str) -> int | None:
+    """Pointer of an optional 64-bit device counter (the saturation count)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype not in (torch.int64, torch.uint64) or t.numel() < 1:
+        raise ValueError(f"{name} must be an int64 tensor of at least one element")
+    return _p(t)
 
 
 def _stream(stream) -> int | None:
@@ -103,8 +127,8 @@ def _rows_cols(x: torch.Tensor):
 
 def fp8_amax(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):
     """amax_out[0] = max|x|; with scale_out / scale_inv_out, also the current scale."""
-    _check(library().fp8_amax(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
-                              _p(scale_out), _p(scale_inv_out), _stream(stream)))
+    _check(library().fp8_amax(_p(x), _dt(x), x.numel(), _f32(amax_out, "amax_out"), fmt, margin,
+                              _f32(scale_out, "scale_out"), _f32(scale_inv_out, "scale_inv_out"), _stream(stream)))
 
 
 def fp8_quantize_mx(x, fmt, q_row=None, scale_row=None, q_col=None, scale_col=None, stream=None):
@@ -136,8 +160,8 @@ def fp8_block128_scales_to_mx(scale_inv, rows, cols, mx_scales, bad_blocks_out=N
         raise TypeError("scale_inv must be float32 and mx_scales uint8")
     if tuple(mx_scales.shape) != (rows, -(-cols // 32)):
         raise ValueError("mx_scales must be uint8 [rows, ceil(cols/32)]")
-    _check(library().fp8_block128_scales_to_mx(_p(scale_inv), rows, cols, _p(mx_scales), _p(bad_blocks_out),
-                                               _stream(stream)))
+    _check(library().fp8_block128_scales_to_mx(_p(scale_inv), rows, cols, _p(mx_scales),
+                                               _u64(bad_blocks_out, "bad_blocks_out"), _stream(stream)))
 
 
 def fp8_amax_noalloc(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_out=None, stream=None):
@@ -145,8 +169,9 @@ def fp8_amax_noalloc(x, amax_out, fmt=E4M3, margin=0, scale_out=None, scale_inv_
     uses a fixed file-scope scratch array instead of a per-stream workspace.
     At most 2**28 elements; make the first call on a device before any stream
     capture; calls that overlap on the GPU race on the shared scratch."""
-    _check(library().fp8_amax_noalloc(_p(x), _dt(x), x.numel(), _p(amax_out), fmt, margin,
-                                      _p(scale_out), _p(scale_inv_out), _stream(stream)))
+    _check(library().fp8_amax_noalloc(_p(x), _dt(x), x.numel(), _f32(amax_out, "amax_out"), fmt, margin,
+                                      _f32(scale_out, "scale_out"), _f32(scale_inv_out, "scale_inv_out"),
+                                      _stream(stream)))
 
 
 def fp8_update_scale_delayed(amax_history, step, new_amax, algo, fmt, margin, scale_out, scale_inv_out,
@@ -154,8 +179,9 @@ def fp8_update_scale_delayed(amax_history, step, new_amax, algo, fmt, margin, sc
     """Delayed-scaling update of a float32 history (in place) -> scale_out, scale_inv_out."""
     if amax_history.dtype != torch.float32:
         raise TypeError("amax_history must be float32")
-    _check(library().fp8_update_scale_delayed(_p(amax_history), amax_history.numel(), int(step), _p(new_amax),
-                                              algo, fmt, margin, _p(scale_out), _p(scale_inv_out),
+    _check(library().fp8_update_scale_delayed(_p(amax_history), amax_history.numel(), int(step),
+                                              _f32(new_amax, "new_amax"), algo, fmt, margin,
+                                              _f32(scale_out, "scale_out"), _f32(scale_inv_out, "scale_inv_out"),
                                               _stream(stream)))
 
 
@@ -165,8 +191,9 @@ def fp8_quantize(x, fmt, scale, q_out, amax_out=None, sat_count_out=None, stream
         raise TypeError("q_out must be uint8")
     if q_out.numel() != x.numel():
         raise ValueError("q_out must have as many elements as x")
-    _check(library().fp8_quantize(_p(x), _dt(x), x.numel(), fmt, _p(scale), _p(q_out), _p(amax_out),
-                                  _p(sat_count_out), _stream(stream)))
+    _check(library().fp8_quantize(_p(x), _dt(x), x.numel(), fmt, _f32(scale, "scale"), _p(q_out),
+                                  _f32(amax_out, "amax_out"), _u64(sat_count_out, "sat_count_out"),
+                                  _stream(stream)))
 
 
 def fp8_quantize_delayed(x, fmt, scale, scale_inv, q_out, amax_history, step, algo=AMAX_MAX, margin=0,
@@ -179,9 +206,10 @@ def fp8_quantize_delayed(x, fmt, scale, scale_inv, q_out, amax_history, step, al
         raise ValueError("q_out must be uint8 with as many elements as x")
     if amax_history.dtype != torch.float32:
         raise TypeError("amax_history must be float32")
-    _check(library().fp8_quantize_delayed(_p(x), _dt(x), x.numel(), fmt, _p(scale), _p(scale_inv), _p(q_out),
-                                          _p(amax_history), amax_history.numel(), int(step), algo, margin,
-                                          _p(amax_out), _p(sat_count_out), _stream(stream)))
+    _check(library().fp8_quantize_delayed(_p(x), _dt(x), x.numel(), fmt, _f32(scale, "scale"),
+                                          _f32(scale_inv, "scale_inv"), _p(q_out), _p(amax_history),
+                                          amax_history.numel(), int(step), algo, margin, _f32(amax_out, "amax_out"),
+                                          _u64(sat_count_out, "sat_count_out"), _stream(stream)))
 
 
 def fp8_quantize_cast_transpose(x, fmt, scale, q_row, q_col, amax_out=None, stream=None):
@@ -191,8 +219,8 @@ def fp8_quantize_cast_transpose(x, fmt, scale, q_row, q_col, amax_out=None, stre
         raise ValueError("q_row must be uint8 [rows, cols]")
     if q_col is not None and (q_col.dtype != torch.uint8 or tuple(q_col.shape) != (cols, rows)):
         raise ValueError("q_col must be uint8 [cols, rows]")
-    _check(library().fp8_quantize_cast_transpose(_p(x), _dt(x), rows, cols, fmt, _p(scale), _p(q_row),
-                                                 _p(q_col), _p(amax_out), _stream(stream)))
+    _check(library().fp8_quantize_cast_transpose(_p(x), _dt(x), rows, cols, fmt, _f32(scale, "scale"), _p(q_row),
+                                                 _p(q_col), _f32(amax_out, "amax_out"), _stream(stream)))
 
 
 def fp8_quantize_block(x, block_rows, block_cols, fmt, q_out, scale_inv_out, stream=None):
@@ -220,7 +248,14 @@ def fp8_dequantize(q, fmt, scale_inv, y, block_rows=0, block_cols=0, stream=None
         if block_rows or block_cols:
             raise ValueError("block-scaled dequantize needs a 2-D q")
         rows, cols = 1, q.numel()
-    _check(library().fp8_dequantize(_p(q), fmt, rows, cols, _p(scale_inv), block_rows, block_cols, _p(y),
+    if block_rows > 0 and block_cols > 0:
+        nblocks = -(-rows // block_rows) * -(-cols // block_cols)
+        if scale_inv.dtype != torch.float32 or scale_inv.numel() < nblocks:
+            raise ValueError(f"block scale_inv must be float32 with at least {nblocks} elements")
+        si = _p(scale_inv)
+    else:
+        si = _f32(scale_inv, "scale_inv")
+    _check(library().fp8_dequantize(_p(q), fmt, rows, cols, si, block_rows, block_cols, _p(y),
                                     _dt(y), _stream(stream)))
 
 
@@ -233,8 +268,9 @@ def fp8_quantize_hybrid(x, fmt_row, scale_row, q_row, fmt_col, scale_col, q_col,
         raise ValueError("q_row must be uint8 [rows, cols]")
     if q_col.dtype != torch.uint8 or tuple(q_col.shape) != (cols, rows):
         raise ValueError("q_col must be uint8 [cols, rows]")
-    _check(library().fp8_quantize_hybrid(_p(x), _dt(x), rows, cols, fmt_row, _p(scale_row), _p(q_row), fmt_col,
-                                         _p(scale_col), _p(q_col), source, _stream(stream)))
+    _check(library().fp8_quantize_hybrid(_p(x), _dt(x), rows, cols, fmt_row, _f32(scale_row, "scale_row"),
+                                         _p(q_row), fmt_col, _f32(scale_col, "scale_col"), _p(q_col), source,
+                                         _stream(stream)))
 
 
 def fp8_quantize_block_cast_transpose(x, fmt, q_row=None, scale_inv_row=None, q_col=None, scale_inv_col=None,
@@ -288,5 +324,6 @@ def fp8_quantize_current(x, fmt, q_out, margin=0, amax_out=None, scale_out=None,
         raise TypeError("q_out must be uint8")
     if q_out.numel() != x.numel():
         raise ValueError("q_out must have as many elements as x")
-    _check(library().fp8_quantize_current(_p(x), _dt(x), x.numel(), fmt, margin, _p(q_out), _p(amax_out),
-                                          _p(scale_out), _p(scale_inv_out), _stream(stream)))
+    _check(library().fp8_quantize_current(_p(x), _dt(x), x.numel(), fmt, margin, _p(q_out),
+                                          _f32(amax_out, "amax_out"), _f32(scale_out, "scale_out"),
+                                          _f32(scale_inv_out, "scale_inv_out"), _stream(stream)))
