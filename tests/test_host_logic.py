@@ -244,3 +244,28 @@ def test_input_digests_hash_each_workloads_bytes():
         h.update(t.view(torch.int16).numpy().tobytes())
     assert d["W3"] == h.hexdigest()[:16]
     assert set(d) == {"W1", "W2", "W3", "W4", "W5"} and len(set(d.values())) == 5
+
+
+def test_bench_parity_check_reports_bit_exact_and_mismatches():
+    """bench.py checks the timed step's outputs against the oracle's in its CPU
+    baseline leg: identical outputs read bit-exact, one flipped byte is named."""
+    import copy
+    import numpy as np
+    import bench
+    from fp8_scaled_quantization_gb300 import workloads as wl
+    inp = {"w1": wl.w1_outliers((64, 128)), "w2": wl.w2_student_t((128, 256)),
+           "w3": list(wl.w3_steps((64, 256), 3)), "w4": wl.w4_block((256, 256), (64, 384)),
+           "w5": list(wl.w5_gradients((64, 512), 2))}
+    host = bench.host_sample(inp, 1.0, max_w3=3, max_w5=2)
+    ref = {}
+    nbytes = bench.oracle_suite_sample(host, 1.0, 2, ref)
+    assert nbytes > 0 and set(ref) == {"W1", "W2", "W3", "W4", "W5"}
+    snap = {w: {k: np.array(v, copy=True).reshape(-1) if np.ndim(v) == 0 else np.array(v, copy=True)
+                for k, v in d.items()} for w, d in ref.items()}
+    out = bench.compare_parity(snap, ref)
+    assert all(out[w] == "bit-exact" for w in ("W1", "W2", "W3", "W4", "W5")), out
+    bad = copy.deepcopy(snap)
+    bad["W4"]["q_a"].reshape(-1)[17] ^= 1
+    bad["W3"]["sat"][1] += 1
+    out = bench.compare_parity(bad, ref)
+    assert out["W4"] == "MISMATCH: q_a" and out["W3"] == "MISMATCH: sat" and out["W1"] == "bit-exact"
