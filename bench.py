@@ -708,6 +708,29 @@ def run_extras(inp, peak, reps=20):
     us = e0.elapsed_time(e1) / 200 * 1e3
     out["w1_graph_warm_l2"] = row(us, x1.numel() * 3, "W1 current scaling (fp8_quantize_current), 20 calls per "
                                   "CUDA graph, warm L2; compulsory 3 B/element")
+    # W1 as it runs in the step: issued right behind a large kernel, so its
+    # launch overlaps that kernel's tail and its input is out of L2; the time
+    # of (large kernel + W1) minus that of the large kernel alone, medians of 20
+    big = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+
+    def pair_us(with_w1):
+        ts = []
+        for r in range(22):
+            e0.record()
+            big.mul_(1.0)
+            if with_w1:
+                fq.fp8_quantize_current(x1, fq.E4M3, q1, 0, a1, s1, si1)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    us = pair_us(True) - pair_us(False)
+    out["w1_behind_large_kernel"] = row(us, x1.numel() * 3, "W1 current scaling issued right behind a 256 MB "
+                                        "kernel (launch overlapped, input out of L2): (kernel + W1) - kernel, "
+                                        "medians of 20; compulsory 3 B/element")
+    del big
     del q1
     # 64 expert-sized tensors: grouped current scaling vs per-tensor calls
     g = torch.Generator(device=dev)

@@ -76,12 +76,12 @@ dequant_tensor_kernel(const uint8_t* __restrict__ q, int64_t n, const float* __r
             float a[4], b[4];
             decode4<FMT>(c[k][0], si, a);
             decode4<FMT>(c[k][kCodes / 4 - 1], si, b);
-            stg_stream(y + i * 16, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
+            stg_evict_first(y + i * 16, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
                                               f32x2_to_bf16x2(b[0], b[1]), f32x2_to_bf16x2(b[2], b[3])));
         } else {
             float a[4];
             decode4<FMT>(c[k][0], si, a);
-            stg_stream(y + i * 16, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+            stg_evict_first(y + i * 16, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
                                               __float_as_uint(a[3])));
         }
     }
@@ -112,11 +112,11 @@ dequant_rows_kernel(const uint8_t* __restrict__ q, int64_t rows, int64_t cols, c
                     float b[4];
                     decode4<FMT>(v.x, si, a);
                     decode4<FMT>(v.y, si, b);
-                    stg_stream(y + e * 2, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
+                    stg_evict_first(y + e * 2, make_uint4(f32x2_to_bf16x2(a[0], a[1]), f32x2_to_bf16x2(a[2], a[3]),
                                                      f32x2_to_bf16x2(b[0], b[1]), f32x2_to_bf16x2(b[2], b[3])));
                 } else {
                     decode4<FMT>(__ldcs(reinterpret_cast<const unsigned int*>(q + e)), si, a);
-                    stg_stream(y + e * 4, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                    stg_evict_first(y + e * 4, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
                                                      __float_as_uint(a[3])));
                 }
             }

@@ -340,6 +340,17 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
                  : "memory");
 }
 
+// Evict-first (streaming) 16-byte store, for outputs that the same chain of
+// kernels does not read again (the dequantized values): their dirty lines
+// leave L2 while the storing kernel runs instead of during the next kernel's
+// reads.  Measured on the E5M2 gradient chain (32 x 8192^2 cast + dequantize):
+// 5% less time than plain stores; the codes keep plain stores because the
+// dequantize reads them back from L2.
+__device__ __forceinline__ void stg_evict_first(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void stg_stream(void* p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }

@@ -270,13 +270,13 @@ mx_dequant_vec_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
             f[4 * w + 3] = __fmul_rn(f16_hi_to_f32(h23), m);
         }
         if constexpr (OUT_BF16) {
-            stg_stream(y + i * 16, make_uint4(f32x2_to_bf16x2(f[0], f[1]), f32x2_to_bf16x2(f[2], f[3]),
+            stg_evict_first(y + i * 16, make_uint4(f32x2_to_bf16x2(f[0], f[1]), f32x2_to_bf16x2(f[2], f[3]),
                                               f32x2_to_bf16x2(f[4], f[5]), f32x2_to_bf16x2(f[6], f[7])));
         } else {
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) o[j] = isnan(f[j]) ? 0x7FFFFFFFu : __float_as_uint(f[j]);
-            stg_stream(y + i * 16, make_uint4(o[0], o[1], o[2], o[3]));
+            stg_evict_first(y + i * 16, make_uint4(o[0], o[1], o[2], o[3]));
         }
     }
 }

@@ -109,3 +109,28 @@ def test_current_in_a_captured_graph(cuda, oracle):
 def test_current_above_the_cast_reduction_threshold(cuda, oracle, dtype, n):
     """Just above 256 amax partials the call switches to amax + finalize + cast."""
     check_against_oracle(oracle, random_input(n, dtype, 90, cuda), E4M3, 1)
+
+
+@pytest.mark.parametrize("dtype,n", [
+    (torch.bfloat16, 8), (torch.bfloat16, 65536 - 1), (torch.bfloat16, 65536), (torch.bfloat16, 65537),
+    (torch.bfloat16, 3 * 65536 + 5), (torch.bfloat16, 9 * 65536 + 3), (torch.bfloat16, (1 << 20) - 7),
+    (torch.bfloat16, 1 << 20), (torch.bfloat16, (1 << 20) + 1),
+    (torch.float32, 4), (torch.float32, 32768 + 1), (torch.float32, 5 * 32768 + 2), (torch.float32, 1 << 19),
+    (torch.float32, (1 << 19) + 3)])
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_current_small_tensor_sizes(cuda, oracle, dtype, fmt, n):
+    """Small tensors: sizes around whole chunks of the amax kernel and of the
+    cast, 2 MiB, and ragged tails, with special values planted."""
+    x = with_specials(random_input(n, dtype, 500 + n, cuda), n)
+    check_against_oracle(oracle, x, fmt, 0)
+    check_against_oracle(oracle, random_input(n, dtype, 600 + n, cuda), fmt, 2)
+
+
+def test_current_planted_maximum_positions(cuda, oracle):
+    """The amax sits in the ragged tail, in the last chunk and in an inner chunk."""
+    for pos in (1048574, 1048555, 948575):
+        x = random_input(1048575, torch.bfloat16, 77, cuda, spread=False)  # |x| < 1000
+        x[pos] = -32768.0  # exact in BF16
+        q, am, s, si = run_current(x, E4M3, 0)
+        assert am == 32768.0
+        check_against_oracle(oracle, x, E4M3, 0)
