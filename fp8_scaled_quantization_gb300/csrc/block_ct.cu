@@ -11,13 +11,17 @@
 //
 // Fast path (BF16, rows % 128 == 0, cols % 128 == 0, 16-byte aligned): one CTA
 // per 128 x 128 tile; each thread holds 8 rows x 8 columns of x in registers.
-//   rows:    the 16 lanes sharing a row reduce its 1 x 128 amax by shuffles;
-//            8 lanes each derive one row's scale (one division) and shuffle it.
-//   columns: each thread folds its 8 rows per column, a 16 x 128 shared table
-//            completes the 128-row reduction, 128 threads derive the scales;
-//            two rows of a column share its scale, so one two-value cvt gives
-//            both codes; the codes go through a swizzled byte-transpose tile
-//            (16-byte stores, full lines).
+//   rows:    the 16 lanes sharing a row reduce its 1 x 128 amax by shuffles,
+//            two rows per 32-bit word (u16x2); 8 lanes each derive one row's
+//            scale and shuffle it.
+//   columns: each thread folds its 8 rows per column pair (u16x2), a 16 x 64
+//            shared table completes the 128-row reduction, 64 threads derive
+//            two column scales each; two rows of a column share its scale, so
+//            one two-lane multiply and one two-value cvt give both codes; the
+//            codes go through a swizzled byte-transpose tile (16-byte stores,
+//            full lines).
+//   Scales come from block_scale_bf16 (exact tables, no division); the
+//   element-exact fixup runs only for a row or tile holding Inf / NaN.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -44,9 +48,11 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads, 4)
 block_ct_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                 float* __restrict__ si_row, uint8_t* __restrict__ q_col, float* __restrict__ si_col) {
+    const uint32_t tword = table_word<FMT>(threadIdx.x);
     pdl_begin();
     __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];  // columnwise codes, swizzled
-    __shared__ uint32_t colmax[16][kTile];                       // per row-group partial column amax (f32 bits)
+    __shared__ uint32_t tab[256];
+    __shared__ __align__(16) uint32_t colmax2[16][kTile / 2];    // per row group: column-pair maxima (u16x2)
     __shared__ float colscale[kTile];
     const int64_t nbr_row = cols / 128, nbr_col = rows / 128;
     const int64_t r0 = (int64_t)blockIdx.x / nbr_row * kTile, c0 = (int64_t)blockIdx.x % nbr_row * kTile;
@@ -55,72 +61,80 @@ block_ct_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
     uint4 v[8];  // v[p]: row p * 16 + rsub, columns cc * 8 .. cc * 8 + 7
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = ldg_stream(x + ((r0 + p * 16 + rsub) * cols + c0 + cc * 8) * 2);
+    tab[t] = tword;
+    __syncthreads();
 
-    // ---- rowwise 1 x 128 tiles: the half-warp of 16 lanes holds one row per p
-    uint32_t rmax[8];
+    // ---- rowwise 1 x 128 tiles: the half-warp of 16 lanes holds one row per p.
+    // Rows p = 2j and 2j + 1 share a word (low / high 16 bits of their |x| bit
+    // patterns), so one u16x2 shuffle-max reduction serves two rows.
+    uint32_t rm2[4];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        uint32_t b = fold_u16x2_to_f32bits(max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
-                                                     max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w))));
+    for (int j = 0; j < 4; ++j) {
+        const uint4 a = v[2 * j], b = v[2 * j + 1];
+        const uint32_t ma = max_u16x2(max_u16x2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
+                                      max_u16x2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
+        const uint32_t mb = max_u16x2(max_u16x2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
+                                      max_u16x2(abs_bf16x2(b.z), abs_bf16x2(b.w)));
+        uint32_t w = max_u16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) b = umax(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
-        rmax[p] = b;
+        for (int o = 8; o > 0; o >>= 1) w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+        rm2[j] = w;
     }
-    uint32_t mine = rmax[0];
+    uint32_t mine2 = rm2[0];
 #pragma unroll
-    for (int p = 1; p < 8; ++p) mine = (cc == p) ? rmax[p] : mine;
-    float rs, rsi;
-    scale_from_amax<FMT>(__uint_as_float(mine), 0, &rs, &rsi);  // lane cc < 8: the scale of row p = cc
+    for (int j = 1; j < 4; ++j) mine2 = (cc >> 1) == j ? rm2[j] : mine2;
+    float rs, rsi;  // lane cc < 8: the scale of row p = cc
+    block_scale_bf16<FMT>(tab, (cc & 1) ? (mine2 & 0xFFFF0000u) : (mine2 << 16), &rs, &rsi);
     if (q_row != nullptr && cc < 8) si_row[(r0 + cc * 16 + rsub) * nbr_row + (c0 >> 7)] = rsi;
 
-    // ---- column partial maxima over this thread's 8 rows
+    // ---- column partial maxima over this thread's 8 rows (column pairs as u16x2)
     if (q_col != nullptr) {
-        uint32_t cm[4] = {0u, 0u, 0u, 0u};  // u16x2: columns (2k, 2k + 1) of the thread's 8
+        uint4 cm = make_uint4(0u, 0u, 0u, 0u);  // columns (2k, 2k + 1) of the thread's 8 in word k
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-            cm[0] = max_u16x2(cm[0], abs_bf16x2(v[p].x));
-            cm[1] = max_u16x2(cm[1], abs_bf16x2(v[p].y));
-            cm[2] = max_u16x2(cm[2], abs_bf16x2(v[p].z));
-            cm[3] = max_u16x2(cm[3], abs_bf16x2(v[p].w));
+            cm.x = max_u16x2(cm.x, abs_bf16x2(v[p].x));
+            cm.y = max_u16x2(cm.y, abs_bf16x2(v[p].y));
+            cm.z = max_u16x2(cm.z, abs_bf16x2(v[p].z));
+            cm.w = max_u16x2(cm.w, abs_bf16x2(v[p].w));
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            colmax[rsub][cc * 8 + 2 * k] = (cm[k] & 0xFFFFu) << 16;
-            colmax[rsub][cc * 8 + 2 * k + 1] = cm[k] & 0xFFFF0000u;
-        }
+        *reinterpret_cast<uint4*>(&colmax2[rsub][cc * 4]) = cm;
     }
 
-    // ---- rowwise codes
+    // ---- rowwise codes; the element-exact fixup only for a row holding Inf / NaN
     if (q_row != nullptr) {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             const float scale = __shfl_sync(0xFFFFFFFFu, rs, (lane & 16) | p);
-            uint32_t m;
-            Codes8 c = cvt_bf16x8<FMT>(v[p], scale, &m);
-            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[p], scale, &c);
+            const uint32_t rmax = (p & 1) ? (rm2[p >> 1] & 0xFFFF0000u) : (rm2[p >> 1] << 16);
+            Codes8 c = cvt_bf16x8_nomax<FMT>(v[p], scale);
+            if (rmax >= 0x7F800000u) fixup_bf16x8<FMT>(v[p], scale, &c);
             stg_stream(q_row + (r0 + p * 16 + rsub) * cols + c0 + cc * 8, make_uint2(c.lo, c.hi));
         }
     }
     if (q_col == nullptr) return;
 
-    // ---- column scales; `special`: some column of the tile holds Inf / NaN
+    // ---- column scales, two columns per thread; `special`: some column of the
+    // tile holds Inf / NaN
     __syncthreads();
-    uint32_t cb = 0;
-    if (t < kTile) {
+    uint32_t cb2 = 0;
+    if (t < kTile / 2) {
 #pragma unroll
-        for (int g = 0; g < 16; ++g) cb = umax(cb, colmax[g][t]);
-        float s, si;
-        scale_from_amax<FMT>(__uint_as_float(cb), 0, &s, &si);
-        colscale[t] = s;
-        si_col[(c0 + t) * nbr_col + (r0 >> 7)] = si;
+        for (int g = 0; g < 16; ++g) cb2 = max_u16x2(cb2, colmax2[g][t]);
+        float s0, si0, s1, si1;
+        block_scale_bf16<FMT>(tab, cb2 << 16, &s0, &si0);
+        block_scale_bf16<FMT>(tab, cb2 & 0xFFFF0000u, &s1, &si1);
+        *reinterpret_cast<float2*>(&colscale[2 * t]) = make_float2(s0, s1);
+        si_col[(c0 + 2 * t) * nbr_col + (r0 >> 7)] = si0;
+        si_col[(c0 + 2 * t + 1) * nbr_col + (r0 >> 7)] = si1;
     }
-    const int special = __syncthreads_or(t < kTile && cb >= 0x7F800000u);
+    const int special = __syncthreads_or(t < kTile / 2 && ((cb2 & 0xFFFFu) >= 0x7F80u || cb2 >= 0x7F800000u));
 
     // ---- columnwise codes into the swizzled tile, then transposed 16-byte stores.
-    // Rows p and p + 1 of one column share its scale, so one two-value cvt gives
-    // both codes; byte permutes then form each row's 4-byte words.  With no
-    // Inf / NaN in a column, |x * scale| <= its amax * scale, so the
-    // round-to-nearest-even saturating cvt is the exact per-element rule.
+    // Rows p and p + 1 of one column share its scale, so one two-lane multiply
+    // and one two-value cvt give both codes; byte permutes then form each
+    // row's 4-byte words.  With no Inf / NaN in a column, |x * scale| <= its
+    // amax * scale, so the round-to-nearest-even saturating cvt is the exact
+    // per-element rule.
     float cs[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) cs[j] = colscale[cc * 8 + j];
@@ -132,10 +146,9 @@ block_ct_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
             uint32_t pr[4];  // pr[h]: bytes (row p, col 2h), (row p+1, col 2h), (row p, col 2h+1), (row p+1, col 2h+1)
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const uint32_t e0 = cvt2<FMT>(__fmul_rn(bf16lo(a[h]), cs[2 * h]), __fmul_rn(bf16lo(bq[h]), cs[2 * h]));
-                const uint32_t e1 =
-                    cvt2<FMT>(__fmul_rn(bf16hi(a[h]), cs[2 * h + 1]), __fmul_rn(bf16hi(bq[h]), cs[2 * h + 1]));
-                pr[h] = __byte_perm(e0, e1, 0x5410);
+                const float2 l = fmul2_rn(bf16lo(a[h]), bf16lo(bq[h]), cs[2 * h]);
+                const float2 u = fmul2_rn(bf16hi(a[h]), bf16hi(bq[h]), cs[2 * h + 1]);
+                pr[h] = __byte_perm(cvt2<FMT>(l.x, l.y), cvt2<FMT>(u.x, u.y), 0x5410);
             }
             const uint32_t lo0 = __byte_perm(pr[0], pr[1], 0x6420), lo1 = __byte_perm(pr[0], pr[1], 0x7531);
             const uint32_t hi0 = __byte_perm(pr[2], pr[3], 0x6420), hi1 = __byte_perm(pr[2], pr[3], 0x7531);

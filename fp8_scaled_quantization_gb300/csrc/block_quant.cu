@@ -13,7 +13,10 @@
 //   128 x 128: one CTA of 256 threads per block, 64 elements per thread.
 //   1 x 128:   one half-warp per tile, 8 elements per lane, eight tiles in
 //              flight per half-warp; the eight scales are computed one per
-//              lane and shuffled back, so each lane does one division.
+//              lane and shuffled back.
+// Block scales of BF16 data come from block_scale_bf16 (exact tables, no
+// division); the element-exact fixup runs only in blocks whose amax is Inf /
+// NaN, decided once per block from the amax already reduced.
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -28,9 +31,11 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q,
                 float* __restrict__ scale_inv, int64_t nbc, int vec_ok) {
+    const uint32_t tword = BF16 ? table_word<FMT>(threadIdx.x) : 0u;
     pdl_begin();
     __shared__ uint32_t red[32];
     __shared__ float s_scale;
+    __shared__ uint32_t tab[256];
     const int64_t bid = blockIdx.x;  // block (bid / nbc, bid % nbc) of the row-major block grid
     const int64_t r0 = bid / nbc * 128, c0 = bid % nbc * 128;
     const int t = threadIdx.x;
@@ -42,6 +47,7 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
         uint4 v[8];
 #pragma unroll
         for (int p = 0; p < 8; ++p) v[p] = ldg_stream(src + (int64_t)p * 16 * cols * 2);
+        tab[t] = tword;  // visible to thread 0 after block_max_u32's barriers
         uint32_t m16 = 0;
 #pragma unroll
         for (int p = 0; p < 8; ++p)
@@ -50,18 +56,18 @@ block128_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8
         const uint32_t bits = block_max_u32(fold_u16x2_to_f32bits(m16), red);
         if (t == 0) {
             float sc, si;  // a NaN amax (bits above Inf) gets scale 1 from the scale rule
-            scale_from_amax<FMT>(__uint_as_float(bits), 0, &sc, &si);
+            block_scale_bf16<FMT>(tab, bits, &sc, &si);
             s_scale = sc;
             scale_inv[bid] = si;
         }
         __syncthreads();
         const float scale = s_scale;
+        const bool special = bits >= 0x7F800000u;  // the block holds Inf / NaN: element-exact codes
         uint8_t* dst = q + (r0 + rsub) * cols + c0 + cc * 8;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-            uint32_t m;
-            Codes8 c = cvt_bf16x8<FMT>(v[p], scale, &m);
-            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[p], scale, &c);
+            Codes8 c = cvt_bf16x8_nomax<FMT>(v[p], scale);
+            if (special) fixup_bf16x8<FMT>(v[p], scale, &c);
             stg_stream(dst + (int64_t)p * 16 * cols, make_uint2(c.lo, c.hi));
         }
         return;
@@ -111,34 +117,51 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
 row128_bf16_kernel(const uint8_t* __restrict__ x, int64_t ntiles, uint8_t* __restrict__ q,
                    float* __restrict__ scale_inv) {
+    __shared__ uint32_t tab[256];
+    const uint32_t tword = table_word<FMT>(threadIdx.x);
     pdl_begin();
     const int t = threadIdx.x;
     const int hw = t >> 4, l16 = t & 15;
     const int lane = t & 31;
+    bool tab_ready = false;
     constexpr int kTilesPerCta = (kThreads / 16) * kTilesInFlight;
     for (int64_t base = (int64_t)blockIdx.x * kTilesPerCta; base < ntiles; base += (int64_t)gridDim.x * kTilesPerCta) {
         uint4 v[kTilesInFlight];
-        uint32_t amx[kTilesInFlight];
 #pragma unroll
         for (int k = 0; k < kTilesInFlight; ++k) {
             const int64_t tile = base + k * 16 + hw;
             v[k] = tile < ntiles ? ldg_stream(x + tile * 256 + l16 * 16) : make_uint4(0, 0, 0, 0);
         }
+        if (!tab_ready) {  // first chunk (every thread of the CTA walks the same chunks)
+            tab[t] = tword;
+            __syncthreads();
+            tab_ready = true;
+        }
+        // Tile amax: two tiles per 32-bit word (tile 2j in the low half, 2j + 1
+        // in the high half, each the top 16 bits of its |x| bit pattern), so one
+        // u16x2 shuffle-max reduction over the half-warp serves two tiles.
+        uint32_t amx2[kTilesInFlight / 2];
 #pragma unroll
-        for (int k = 0; k < kTilesInFlight; ++k) {
-            uint32_t m = max_u16x2(max_u16x2(abs_bf16x2(v[k].x), abs_bf16x2(v[k].y)),
-                                   max_u16x2(abs_bf16x2(v[k].z), abs_bf16x2(v[k].w)));
-            uint32_t b = fold_u16x2_to_f32bits(m);
+        for (int j = 0; j < kTilesInFlight / 2; ++j) {
+            const uint4 a = v[2 * j], b = v[2 * j + 1];
+            const uint32_t ma = max_u16x2(max_u16x2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
+                                          max_u16x2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
+            const uint32_t mb = max_u16x2(max_u16x2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
+                                          max_u16x2(abs_bf16x2(b.z), abs_bf16x2(b.w)));
+            // low halves of ma / mb in one word, high halves in another: the max
+            // of the two words is (amax of tile 2j, amax of tile 2j + 1)
+            uint32_t w = max_u16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) b = umax(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
-            amx[k] = b;
+            for (int o = 8; o > 0; o >>= 1) w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+            amx2[j] = w;
         }
         // Lane l16 < kTilesInFlight of each half-warp derives the scale of tile k = l16.
-        uint32_t mine = amx[0];
+        uint32_t mine2 = amx2[0];
 #pragma unroll
-        for (int k = 1; k < kTilesInFlight; ++k) mine = (l16 == k) ? amx[k] : mine;
+        for (int j = 1; j < kTilesInFlight / 2; ++j) mine2 = (l16 >> 1) == j ? amx2[j] : mine2;
+        const uint32_t mine = (l16 & 1) ? (mine2 & 0xFFFF0000u) : (mine2 << 16);
         float sc, si;
-        scale_from_amax<FMT>(__uint_as_float(mine), 0, &sc, &si);
+        block_scale_bf16<FMT>(tab, mine, &sc, &si);
         if (l16 < kTilesInFlight) {
             const int64_t tile = base + l16 * 16 + hw;
             if (tile < ntiles) scale_inv[tile] = si;
@@ -148,9 +171,9 @@ row128_bf16_kernel(const uint8_t* __restrict__ x, int64_t ntiles, uint8_t* __res
             const float scale = __shfl_sync(0xFFFFFFFFu, sc, (lane & 16) | k);
             const int64_t tile = base + k * 16 + hw;
             if (tile >= ntiles) continue;
-            uint32_t m;
-            Codes8 c = cvt_bf16x8<FMT>(v[k], scale, &m);
-            if (chunk_needs_fixup<FMT, false>(fold_u16x2_to_f32bits(m), scale)) fixup_bf16x8<FMT>(v[k], scale, &c);
+            const uint32_t tmax = (k & 1) ? (amx2[k >> 1] & 0xFFFF0000u) : (amx2[k >> 1] << 16);
+            Codes8 c = cvt_bf16x8_nomax<FMT>(v[k], scale);
+            if (tmax >= 0x7F800000u) fixup_bf16x8<FMT>(v[k], scale, &c);  // the tile holds Inf / NaN
             stg_stream(q + tile * 128 + l16 * 8, make_uint2(c.lo, c.hi));
         }
     }
@@ -161,7 +184,6 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 row128_guarded_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, int64_t nbc,
                       uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
-    pdl_begin();
     pdl_begin();
     const int t = threadIdx.x, hw = t >> 4, l16 = t & 15;
     const int64_t ntiles = rows * nbc;

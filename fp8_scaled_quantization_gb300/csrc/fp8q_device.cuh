@@ -139,6 +139,82 @@ __device__ __forceinline__ float scale_from_amax_rt(int fmt, float amax, int mar
     return s;
 }
 
+// ------------------------------------------- block scales of a BF16 amax
+//
+// A BF16 magnitude a = (1 + i/128) * 2^(E-127) has a 7-bit fraction i, so
+// FP8_MAX / a = T[i] * 2^(127-E) with T[i] = FP8_MAX / (1 + i/128): rounding
+// commutes with the power of two while the result stays a normal fp32
+// number, so RN(FP8_MAX / a) = RN(T[i]) * 2^(127-E), and likewise
+// RN(1 / s) = RN(1 / RN(T[i])) * 2^(E-127).  The two 128-entry tables per
+// format are built at compile time in integer arithmetic with round half to
+// even, so they hold what a correctly rounded fp32 division gives; two table
+// reads and two exponent adds replace the two divisions of the scale rule for
+// every block of BF16 data (margin 0, the block recipes' rule).
+
+// RN-even fp32 bit pattern of num / den for positive integers whose quotient
+// is a normal fp32 number and for which num * 2^48 and den * 2^48 fit in 64 bits.
+constexpr uint32_t rn_quotient_bits(uint64_t num, uint64_t den) {
+    int k = 0;  // quotient = q * 2^-k
+    while (num < (den << 23)) { num <<= 1; ++k; }
+    while (num >= (den << 24)) { den <<= 1; --k; }
+    uint64_t q = num / den;
+    const uint64_t r = num % den;
+    if (2 * r > den || (2 * r == den && (q & 1))) ++q;
+    if (q == (1ull << 24)) { q >>= 1; --k; }
+    return (uint32_t)((150 - k) << 23) | (uint32_t)(q - (1ull << 23));
+}
+
+struct Bf16ScaleTables {
+    uint32_t s[2][128];   // RN(FP8_MAX / (1 + i/128)), per format
+    uint32_t si[2][128];  // RN(1 / s)
+};
+
+constexpr Bf16ScaleTables make_bf16_scale_tables() {
+    Bf16ScaleTables t{};
+    for (int f = 0; f < 2; ++f) {
+        const uint64_t fmax = f == kE4M3 ? 448 : 57344;
+        for (int i = 0; i < 128; ++i) {
+            const uint32_t sb = rn_quotient_bits(fmax * 128, 128 + (uint64_t)i);
+            t.s[f][i] = sb;
+            // s = (2^23 + m) * 2^(e - 150), so 1 / s = 2^(150 - e) / (2^23 + m)
+            t.si[f][i] = rn_quotient_bits(1ull << (150 - (sb >> 23)), (1ull << 23) | (sb & 0x7FFFFFu));
+        }
+    }
+    return t;
+}
+
+static __device__ const Bf16ScaleTables g_bf16_scale_tables = make_bf16_scale_tables();
+
+// One format's tables in shared memory: word i < 128 is s[i], word 128 + i is
+// si[i].  A kernel reads its word of the table (table_word, one per thread of
+// a 256-thread CTA) before its dependency wait -- the tables are constants that
+// no kernel writes -- stores it after issuing its own loads, and synchronises
+// before the first lookup, so the lookups are shared-memory reads.
+template <int FMT>
+__device__ __forceinline__ uint32_t table_word(int t) {
+    return t < 128 ? __ldg(&g_bf16_scale_tables.s[FMT][t]) : __ldg(&g_bf16_scale_tables.si[FMT][t - 128]);
+}
+
+// scale and scale_inv of a block whose amax bits are those of a BF16 value
+// (low 16 bits zero), margin 0, from the shared table `tab`: exactly what
+// scale_from_amax gives.  Any other amax (fp32 data, zero, subnormal, Inf,
+// NaN) and results outside the normal range go through scale_from_amax.
+template <int FMT>
+__device__ __forceinline__ void block_scale_bf16(const uint32_t* tab, uint32_t bits, float* scale, float* scale_inv) {
+    const int e = (int)(bits >> 23);
+    if ((bits & 0xFFFFu) == 0 && e >= 1 && e <= 254) {
+        const uint32_t i = (bits >> 16) & 0x7Fu;
+        const uint32_t sb = tab[i], ib = tab[128 + i];
+        const int es = (int)(sb >> 23) + 127 - e, ei = (int)(ib >> 23) + e - 127;
+        if (es >= 1 && es <= 254 && ei >= 1 && ei <= 254) {
+            *scale = __uint_as_float(((uint32_t)es << 23) | (sb & 0x7FFFFFu));
+            *scale_inv = __uint_as_float(((uint32_t)ei << 23) | (ib & 0x7FFFFFu));
+            return;
+        }
+    }
+    scale_from_amax<FMT>(__uint_as_float(bits), 0, scale, scale_inv);
+}
+
 // ------------------------------------------------------- element-exact path
 
 // One element with every special case spelled out; used by the slow path.
@@ -181,6 +257,20 @@ __device__ __forceinline__ Codes8 cvt_bf16x8(uint4 v, float scale, uint32_t* abs
     return c;
 }
 
+// The same 8 codes without the |x| maximum, for callers that already know
+// whether the values hold Inf / NaN (the block kernels, from the block amax).
+template <int FMT>
+__device__ __forceinline__ Codes8 cvt_bf16x8_nomax(uint4 v, float scale) {
+    Codes8 c;
+    const float2 p0 = fmul2_rn(bf16lo(v.x), bf16hi(v.x), scale);
+    const float2 p1 = fmul2_rn(bf16lo(v.y), bf16hi(v.y), scale);
+    const float2 p2 = fmul2_rn(bf16lo(v.z), bf16hi(v.z), scale);
+    const float2 p3 = fmul2_rn(bf16lo(v.w), bf16hi(v.w), scale);
+    c.lo = cvt2<FMT>(p0.x, p0.y) | (cvt2<FMT>(p1.x, p1.y) << 16);
+    c.hi = cvt2<FMT>(p2.x, p2.y) | (cvt2<FMT>(p3.x, p3.y) << 16);
+    return c;
+}
+
 // True when the chunk needs the element-exact path: some |x| is Inf/NaN, or
 // (when counting saturation) the largest |x| * scale exceeds FP8_MAX.
 template <int FMT, bool COUNT_SAT>
@@ -193,23 +283,37 @@ __device__ __forceinline__ bool chunk_needs_fixup(uint32_t absmax_f32bits, float
     }
 }
 
-// Redo 8 BF16 elements exactly; returns the saturated-element count.
+// Redo 8 BF16 elements exactly.  The out-of-line part returns codes and the
+// saturated count by value, so the caller's code words never need a stack
+// slot (a pointer argument would force them into local memory on every chunk,
+// fixed up or not); the inline wrapper keeps the call sites' form.
+struct Fixed8 {
+    uint32_t lo, hi, sat;
+};
+
 template <int FMT>
-__device__ __noinline__ uint32_t fixup_bf16x8(uint4 v, float scale, Codes8* c) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2] = {0u, 0u};
-    uint32_t sat = 0;
+__device__ __noinline__ Fixed8 fixup_bf16x8_exact(uint4 v, float scale) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    Fixed8 r = {0u, 0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        float x = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+        const float x = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
         uint32_t s;
-        uint32_t code = quant_one<FMT>(x, scale, &s);
-        sat += s;
-        out[i >> 2] |= code << (8 * (i & 3));
+        const uint32_t code = quant_one<FMT>(x, scale, &s);
+        r.sat += s;
+        if (i < 4) r.lo |= code << (8 * i);
+        else r.hi |= code << (8 * (i - 4));
     }
-    c->lo = out[0];
-    c->hi = out[1];
-    return sat;
+    return r;
+}
+
+// Returns the saturated-element count; *c receives the 8 codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t fixup_bf16x8(uint4 v, float scale, Codes8* c) {
+    const Fixed8 r = fixup_bf16x8_exact<FMT>(v, scale);
+    c->lo = r.lo;
+    c->hi = r.hi;
+    return r.sat;
 }
 
 // ----------------------------------------------------------- fp32 inputs
@@ -227,9 +331,10 @@ __device__ __forceinline__ uint32_t cvt_f32x4(float4 v, float scale, uint32_t* a
     return c0 | (c1 << 16);
 }
 
+// Redo 4 fp32 elements exactly (by value, as fixup_bf16x8_exact).
 template <int FMT>
-__device__ __noinline__ uint32_t fixup_f32x4(float4 v, float scale, uint32_t* code4) {
-    float e[4] = {v.x, v.y, v.z, v.w};
+__device__ __noinline__ uint2 fixup_f32x4_exact(float4 v, float scale) {
+    const float e[4] = {v.x, v.y, v.z, v.w};
     uint32_t out = 0, sat = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -237,8 +342,15 @@ __device__ __noinline__ uint32_t fixup_f32x4(float4 v, float scale, uint32_t* co
         out |= quant_one<FMT>(e[i], scale, &s) << (8 * i);
         sat += s;
     }
-    *code4 = out;
-    return sat;
+    return make_uint2(out, sat);
+}
+
+// Returns the saturated-element count; *code4 receives the 4 codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t fixup_f32x4(float4 v, float scale, uint32_t* code4) {
+    const uint2 r = fixup_f32x4_exact<FMT>(v, scale);
+    *code4 = r.x;
+    return r.y;
 }
 
 // ----------------------------------------------------------- reductions

@@ -81,8 +81,9 @@ __device__ __forceinline__ void mx_block_codes(uint32_t bits, uint4 lo, uint4 hi
 
 // NARROW (rows, cols < 2^24): addresses are per-tile 64-bit bases plus 32-bit
 // offsets inside the tile, which saves the 64-bit multiply-adds of every access.
+// 48 registers: 5 CTAs (1280 threads) per SM, 160 KB of tiles in shared memory.
 template <int FMT, bool NARROW>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 5)
 mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
     using Off = typename std::conditional<NARROW, uint32_t, int64_t>::type;
@@ -139,25 +140,36 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
         const int cp = (t >> 3) + 32 * u;  // columns 2 cp, 2 cp + 1
         // rows 16 g .. 16 g + 15 all have (row / 16) % 8 == g, so one chunk swizzle
         const uint32_t* wcol = tw + g * 16 * 64 + mx_chunk(g * 16, cp >> 2) * 4 + (cp & 3);
-        uint32_t w[16];
+        uint32_t w[16];  // w[i]: row 16 g + i, columns 2 cp (low half) and 2 cp + 1 (high half)
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = wcol[i * 64];
+        // Both columns' |x| maxima at once (u16x2), then the other half of the
+        // 32-row block from lane g ^ 1.
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m2 = max_u16x2(m2, abs_bf16x2(w[i]));
+        m2 = max_u16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const uint32_t sel = j ? 0x7632u : 0x5410u;  // high or low halves: column 2 cp + j
-            const uint4 lo = make_uint4(__byte_perm(w[0], w[1], sel), __byte_perm(w[2], w[3], sel),
-                                        __byte_perm(w[4], w[5], sel), __byte_perm(w[6], w[7], sel));
-            const uint4 hi = make_uint4(__byte_perm(w[8], w[9], sel), __byte_perm(w[10], w[11], sel),
-                                        __byte_perm(w[12], w[13], sel), __byte_perm(w[14], w[15], sel));
-            const uint32_t m16 = max_u16x2(max_u16x2(max_u16x2(abs_bf16x2(lo.x), abs_bf16x2(lo.y)),
-                                                     max_u16x2(abs_bf16x2(lo.z), abs_bf16x2(lo.w))),
-                                           max_u16x2(max_u16x2(abs_bf16x2(hi.x), abs_bf16x2(hi.y)),
-                                                     max_u16x2(abs_bf16x2(hi.z), abs_bf16x2(hi.w))));
-            uint32_t bits = fold_u16x2_to_f32bits(m16);
-            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));  // the other half of the 32-row block
+            const uint32_t bits = j ? (m2 & 0xFFFF0000u) : (m2 << 16);  // column 2 cp + j
             uint4 codes;
             uint32_t code;
-            mx_block_codes<FMT>(bits, lo, hi, &codes, &code);
+            if (bits >= 0x7F800000u) {
+                code = 0xFFu;
+                codes = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            } else {
+                code = mx_scale_code<FMT>(bits);
+                const float mul = mx_multiplier(code);
+                uint32_t c2[8];  // codes of rows 2 i, 2 i + 1
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = j ? fmul2_rn(bf16hi(w[2 * i]), bf16hi(w[2 * i + 1]), mul)
+                                       : fmul2_rn(bf16lo(w[2 * i]), bf16lo(w[2 * i + 1]), mul);
+                    c2[i] = cvt2<FMT>(f.x, f.y);
+                }
+                codes = make_uint4(__byte_perm(c2[0], c2[1], 0x5410), __byte_perm(c2[2], c2[3], 0x5410),
+                                   __byte_perm(c2[4], c2[5], 0x5410), __byte_perm(c2[6], c2[7], 0x5410));
+            }
             const Off c = (Off)(2 * cp + j);  // column inside the tile
             if (live) {
                 stg_stream(qc + (c * orows + (Off)(g * 16)), codes);
