@@ -54,3 +54,24 @@ def test_noalloc_matches_allocating_amax_two_calls_in_a_row(cuda):
             torch.cuda.synchronize()
             ref, got = [_bits(t) for t in out[:3]], [_bits(t) for t in out[3:]]
             assert got == ref, (call, x.numel(), x.dtype)
+
+
+@pytest.mark.gpu
+def test_noalloc_at_its_capacity(cuda):
+    """2^28 BF16 elements (every one of the 4096 scratch slots in use) with the
+    maximum in the last element, and 2^28 - 1 elements starting one element
+    past a 16-byte boundary (the element-at-a-time path), each against
+    fp8_amax bit for bit, two calls in a row."""
+    g = torch.Generator(device=cuda).manual_seed(4321)
+    full = torch.randn(MAX_ELEMS, generator=g, device=cuda).to(torch.bfloat16)
+    full[-1] = -1024.0  # above every N(0, 1) draw: the last CTA's slot holds the maximum
+    cases = [(full, fq.E4M3, 0), (full[1:], fq.E5M2, 2)]
+    for call in range(2):
+        for x, fmt, margin in cases:
+            out = [torch.full((1,), -1.0, device=cuda) for _ in range(6)]
+            fq.fp8_amax(x, out[0], fmt, margin, out[1], out[2])
+            fq.fp8_amax_noalloc(x, out[3], fmt, margin, out[4], out[5])
+            torch.cuda.synchronize()
+            ref, got = [_bits(t) for t in out[:3]], [_bits(t) for t in out[3:]]
+            assert got == ref, (call, x.numel())
+            assert out[3].item() == 1024.0
