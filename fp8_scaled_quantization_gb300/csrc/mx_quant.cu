@@ -47,8 +47,7 @@ __device__ __forceinline__ float mx_multiplier(uint32_t code) { return exp2i(127
 // One block's worth of 8 BF16 values -> 8 codes with the block's multiplier.
 template <int FMT>
 __device__ __forceinline__ uint2 mx_codes8(uint4 v, float m) {
-    uint32_t dummy;
-    const Codes8 c = cvt_bf16x8<FMT>(v, m, &dummy);
+    const Codes8 c = cvt_bf16x8_nomax<FMT>(v, m);
     return make_uint2(c.lo, c.hi);
 }
 
@@ -106,16 +105,32 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
 #pragma unroll
     for (int p = 0; p < kLoads; ++p)
         if (p * 16 < vrows) v[p] = ldg_stream(xt + ((Off)(p * 16 + rsub) * ocols + (Off)(cc * 8)) * 2);
+    // Row blocks: rows p = 2j and 2j + 1 share a word (low / high 16 bits of
+    // their |x| bit patterns), so one u16x2 shuffle-max over the 4 lanes of a
+    // 32-element block serves both rows.  vrows is a multiple of 32, so the
+    // rows of a pair are both inside the tensor or both outside.
+    uint32_t rb2[kLoads / 2] = {};
+    if (q_row) {
+#pragma unroll
+        for (int j = 0; j < kLoads / 2; ++j) {
+            if (2 * j * 16 >= vrows) break;  // uniform over the CTA
+            const uint4 a = v[2 * j], b = v[2 * j + 1];
+            const uint32_t ma = max_u16x2(max_u16x2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
+                                          max_u16x2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
+            const uint32_t mb = max_u16x2(max_u16x2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
+                                          max_u16x2(abs_bf16x2(b.z), abs_bf16x2(b.w)));
+            uint32_t w = max_u16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
+            w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, 1));
+            w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, 2));  // 4 lanes = one 32-element block
+            rb2[j] = w;
+        }
+    }
 #pragma unroll
     for (int p = 0; p < kLoads; ++p) {
         if (p * 16 >= vrows) break;  // uniform over the CTA
         const int r = p * 16 + rsub;
         if (q_row) {
-            uint32_t m16 = max_u16x2(max_u16x2(abs_bf16x2(v[p].x), abs_bf16x2(v[p].y)),
-                                     max_u16x2(abs_bf16x2(v[p].z), abs_bf16x2(v[p].w)));
-            uint32_t bits = fold_u16x2_to_f32bits(m16);
-            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 1));
-            bits = umax(bits, __shfl_xor_sync(0xFFFFFFFFu, bits, 2));  // 4 lanes = one 32-element block
+            const uint32_t bits = (p & 1) ? (rb2[p >> 1] & 0xFFFF0000u) : (rb2[p >> 1] << 16);
             uint2 codes;
             uint32_t code;
             if (bits >= 0x7F800000u) {
