@@ -116,12 +116,16 @@ def make_pipelines(inp):
         pipes["W1"] = P.CurrentScaling(inp["w1"], E4M3, 0)
     if "w2" in inp:
         pipes["W2"] = P.CurrentCastTranspose(inp["w2"], E4M3, 1)
+    # Every W3 step and every W5 tensor writes its own output buffers: with one
+    # buffer reused, a launch would overwrite lines of the previous launch's
+    # output that are still dirty in L2, and those writes would never reach
+    # DRAM (the delayed cast measured 27.5 against 31.4 us back to back).
     if "w3" in inp:
-        pipes["W3"] = P.DelayedScaling(inp["w3"], 1024, E4M3, 0)
+        pipes["W3"] = P.DelayedScaling(inp["w3"], 1024, E4M3, 0, keep_codes=True)
     if "w4" in inp:
         pipes["W4"] = P.BlockScaling(*inp["w4"], E4M3)
     if "w5" in inp:
-        pipes["W5"] = P.GradientQDQ(inp["w5"], E5M2, 0, group=W5_GROUP)
+        pipes["W5"] = P.GradientQDQ(inp["w5"], E5M2, 0, keep_outputs=True, group=W5_GROUP)
     return pipes
 
 
@@ -385,10 +389,13 @@ def run_ours(args, rank, world):
     for name, (fn, nbytes) in back_to_back_calls(pipes, dev).items():
         if name not in kernels:
             continue
-        us = time_back_to_back(fn)
+        small = nbytes < B2B_GRAPH_BELOW_BYTES
+        us = time_back_to_back(fn, graph=small)
         gbs = nbytes / (us * 1e-6) / 1e9
         kernels[name].update({"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "ms_per_step": round(us * kernels[name]["launches_per_step"] * 1e-3, 4)})
+        if small:
+            kernels[name]["timing"] = "CUDA-graph replay of the back-to-back calls (input resident in L2)"
     # The roofline is a single kernel's: the call with the largest share of the
     # step (its event-bracketed time in the step, which keeps what the step's
     # L2 state gives it) among those that are one kernel launch (the reducing
@@ -417,7 +424,8 @@ def run_ours(args, rank, world):
                    "bytes": "compulsory: each workload's inputs read once + outputs written once",
                    "compulsory_bytes_per_step": step_bytes, "kernel_bytes_per_step": kernel_bytes,
                    "kernel_gbs": round(world * kernel_bytes * args.steps / (ms_max * 1e-3) / 1e9, 1),
-                   "l2": "no flush: inputs (%.2f GB) and per-step traffic (%.2f GB) exceed the 135 MB L2"
+                   "l2": "no flush: inputs (%.2f GB) and per-step traffic (%.2f GB) exceed the 135 MB L2; every "
+                         "W3 step and W5 tensor writes its own output buffers"
                          % (sum(t.numel() * t.element_size() for t in _all_inputs(inp)) / 1e9, kernel_bytes / 1e9),
                    "w5_path": "one grouped amax + scale call over the 32 tensors (per-tensor scales), then "
                               "per tensor its cast and its dequantize",
@@ -512,14 +520,42 @@ def back_to_back_calls(pipes, dev):
     return calls
 
 
-def time_back_to_back(fn):
-    """Average per-launch time (us) of B2B_LAUNCHES back-to-back calls, median of B2B_GROUPS groups."""
+# Calls that move less than this are issued faster by the GPU than by the
+# Python binding: their back-to-back launches are replayed from a CUDA graph.
+B2B_GRAPH_BELOW_BYTES = 16 << 20
+
+
+def time_back_to_back(fn, graph=False):
+    """Average per-launch time (us) of B2B_LAUNCHES back-to-back calls, median
+    of B2B_GROUPS groups; with `graph`, the calls are captured once in a CUDA
+    graph on a side stream and the graph is replayed (GPU time, not the host's
+    launch rate)."""
     import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = []
+    if graph:
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            for i in range(3):
+                fn(i)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(B2B_LAUNCHES):
+                    fn(i)
+            g.replay()
+            st.synchronize()
+            for _ in range(B2B_GROUPS):
+                e0.record(st)
+                g.replay()
+                e1.record(st)
+                st.synchronize()
+                per.append(e0.elapsed_time(e1) * 1e3 / B2B_LAUNCHES)
+        torch.cuda.current_stream().wait_stream(st)
+        return statistics.median(per)
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    per = []
     for g in range(B2B_GROUPS):
         e0.record()
         for i in range(B2B_LAUNCHES):
