@@ -362,7 +362,8 @@ fp8_status_t fp8_quantize_grouped(int count, const void* const* xs, const int64_
  *   scale_inv  device float: one value when block_rows = block_cols = 0
  *              (per-tensor), else the [ceil(rows/br), ceil(cols/bc)] block
  *              grid of fp8_quantize_block with (br, bc) = (128,128) or (1,128).
- *   y          device [rows, cols] of out_dtype.
+ *   y          device [rows, cols] of out_dtype, written with evict-first
+ *              (streaming) stores: the values leave L2 as they are written.
  * One kernel launch. */
 fp8_status_t fp8_dequantize(const uint8_t* q, fp8_format_t fmt, int64_t rows, int64_t cols,
                             const float* scale_inv, int block_rows, int block_cols, void* y,
