@@ -30,7 +30,7 @@ __all__ = [
     "fp8_quantize_block", "fp8_dequantize", "fp8_quantize_delayed", "fp8_quantize_mx", "fp8_dequantize_mx",
     "fp8_block128_scales_to_mx", "fp8_amax_noalloc", "fp8_quantize_current", "fp8_quantize_hybrid", "fp8_quantize_block_cast_transpose",
     "fp8_amax_grouped", "fp8_quantize_grouped", "COLUMNWISE_FROM_ORIGINAL", "COLUMNWISE_FROM_ROWWISE_DEQUANTIZED",
-    "launch_count", "version", "library", "release_stream_workspace",
+    "launch_count", "version", "library", "release_stream_workspace", "wait_timeouts",
 ]
 
 
@@ -52,6 +52,16 @@ def version() -> int:
 def launch_count() -> int:
     """Kernels launched by the library so far in this process."""
     return int(library().fp8_launch_count())
+
+
+def wait_timeouts() -> int:
+    """Waits inside the library's tile pipelines that gave up on the current
+    device since the library was loaded (synchronises the device).  Any change
+    across a call means that call's outputs are incomplete."""
+    import ctypes
+    count = ctypes.c_ulonglong(0)
+    _check(library().fp8_wait_timeouts(ctypes.addressof(count)))
+    return int(count.value)
 
 
 def release_stream_workspace(stream=None):

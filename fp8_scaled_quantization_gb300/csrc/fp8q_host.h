@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "fp8q.h"
@@ -22,12 +23,43 @@ fp8_status_t after_launch(const char* kernel);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Tensor map of a row-major [rows, cols] array of 16-bit elements at `base`
+// (16-byte aligned, cols * 2 a multiple of 16, rows and cols at most 2^32),
+// read in boxes of box_rows x box_cols elements into packed shared-memory rows
+// (no swizzle).  The encoder is the driver's, reached through the runtime.
+fp8_status_t encode_tile_map_u16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                                 int box_cols);
+
 // Workspace of (current device, stream) for per-CTA partials; nullptr on
 // failure (the error message is set).
 Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st);
 
-// Launch `kernel` on `st` with programmatic stream serialization allowed (the
-// kernel starts with pdl_begin()), then check and count the launch.
+// Launch `kernel` on `st` with `smem` bytes of dynamic shared memory and
+// programmatic stream serialization allowed (the kernel starts with
+// pdl_begin()), then check and count the launch.
+template <typename... KArgs, typename... Args>
+fp8_status_t launch_smem(const char* what, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t st, Args... args) {
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_status(e, what);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) return cuda_status(e, what);
+    return after_launch(what);
+}
+
+// The same without dynamic shared memory.
 template <typename... KArgs, typename... Args>
 fp8_status_t launch(const char* what, void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
                     Args... args) {

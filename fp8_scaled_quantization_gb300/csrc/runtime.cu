@@ -7,6 +7,8 @@
 #include <mutex>
 #include <utility>
 
+#include <cudaTypedefs.h>
+
 #include "fp8q_device.cuh"
 #include "fp8q_host.h"
 
@@ -51,6 +53,31 @@ int sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     g_sm_count[dev] = n;
     return n;
+}
+
+fp8_status_t encode_tile_map_u16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                                 int box_cols) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return fail(FP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+                              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return FP8_OK;
 }
 
 Workspace* stream_workspace(cudaStream_t stream, fp8_status_t* st) {

@@ -110,6 +110,18 @@ int fp8_version(void);
  * all threads).  Lets a caller count launches inside a timed region. */
 unsigned long long fp8_launch_count(void);
 
+/* Number of waits inside the library's tile pipelines (a consumer waiting for
+ * a tile's bulk copy to land, the copying warp waiting for a stage to be
+ * released) that gave up after their limit of about two seconds, on the
+ * current device, since the library was loaded.  Written to *count after the
+ * device has finished all queued work (the call synchronises the device).  A
+ * wait that gives up never hangs the kernel: the kernel finishes, but the
+ * outputs of that launch are incomplete, so any nonzero change of the count
+ * across a call means that call's outputs must not be used.  Correct inputs
+ * never reach the limit: a stage is always filled and released by the same
+ * launch.  FP8_ERR_INVALID_ARG if count is NULL. */
+fp8_status_t fp8_wait_timeouts(unsigned long long* count);
+
 /* Frees the reduction workspace (96 KB) that the calls made on `stream` on the
  * current device, after waiting for the work queued on that stream.  A later
  * reducing call on the stream allocates a new one.  Returns FP8_OK when there

@@ -629,6 +629,34 @@ def test_block_cast_transpose_matches_oracle(cuda, oracle, dtype, fmt, shape):
     assert np.array_equal(q_col.cpu().numpy(), wqt)
 
 
+@pytest.mark.parametrize("shape", [(128, 128), (384, 128), (1024, 12800), (2048, 20480)])
+@pytest.mark.parametrize("direction", ["both", "rows", "cols"])
+def test_block_cast_transpose_tile_ring(cuda, oracle, shape, direction):
+    """The persistent kernel at tile counts that leave a consumer group idle
+    (1 and 3 tiles), wrap the stage ring (800 tiles: 5 or 6 per CTA) and run
+    16-17 tiles per CTA, with Inf / NaN planted in some tiles; no bounded wait
+    inside the kernel gives up."""
+    rows, cols = shape
+    x = with_specials(random_input(shape, torch.bfloat16, rows + cols, cuda), rows)
+    before = fq.wait_timeouts()
+    want_rows, want_cols = direction != "cols", direction != "rows"
+    q_row = torch.full((rows, cols), 0xAA, dtype=torch.uint8, device=cuda) if want_rows else None
+    s_row = torch.zeros((rows, cols // 128), dtype=torch.float32, device=cuda) if want_rows else None
+    q_col = torch.full((cols, rows), 0xAA, dtype=torch.uint8, device=cuda) if want_cols else None
+    s_col = torch.zeros((cols, rows // 128), dtype=torch.float32, device=cuda) if want_cols else None
+    fq.fp8_quantize_block_cast_transpose(x, E4M3, q_row, s_row, q_col, s_col)
+    assert fq.wait_timeouts() == before
+    xb = host_bits(x)
+    if want_rows:
+        wq, ws = oracle.quantize_block(xb, 1, 128, E4M3)
+        assert np.array_equal(s_row.cpu().numpy().view(np.uint32), ws.view(np.uint32))
+        assert np.array_equal(q_row.cpu().numpy(), wq)
+    if want_cols:
+        wqt, wst = oracle.quantize_block(np.ascontiguousarray(xb.T), 1, 128, E4M3)
+        assert np.array_equal(s_col.cpu().numpy().view(np.uint32), wst.view(np.uint32))
+        assert np.array_equal(q_col.cpu().numpy(), wqt)
+
+
 def test_block_cast_transpose_tile_without_specials(cuda, oracle):
     """A 512 x 512 BF16 tensor with no Inf / NaN: every tile takes the paired
     two-value conversion of the columnwise codes."""

@@ -89,6 +89,7 @@ BAD = 0x1000  # never dereferenced: every call below is rejected on the host fir
     (lambda L: L.fp8_amax_grouped(2, BAD, BAD, 0, None, 0, 0, None, None, None), 1, "no output requested"),
     (lambda L: L.fp8_quantize_grouped(2, None, BAD, 0, 0, BAD, BAD, None), 1, "is NULL"),
     (lambda L: L.fp8_quantize_grouped(2, BAD, BAD, 0, 0, None, BAD, None), 1, "scales is NULL"),
+    (lambda L: L.fp8_wait_timeouts(None), 1, "count is NULL"),
 ])
 def test_host_validation_rejects_before_launch(native_lib, call, status, msg):
     before = native_lib.fp8_launch_count()
