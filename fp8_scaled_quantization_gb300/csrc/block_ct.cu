@@ -267,9 +267,6 @@ transpose:
     }
 }
 
-// Waits that gave up in this file's pipelines (read by fp8_wait_timeouts).
-__device__ unsigned long long g_bct_wait_timeouts;
-
 // Shared memory of the pipelined kernel: S stages of one 128 x 128 BF16 tile
 // (32 KB, rows of 256 bytes), NG group areas, the scale tables, the barriers.
 template <int NG, int S>
@@ -326,7 +323,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
         for (; k < n_my; ++k) {
             const uint32_t s = k % S;
             if (k >= S && !mbar_wait(&empty[s], ((k / S) & 1u) ^ 1u)) {
-                atomicAdd(&g_bct_wait_timeouts, 1ull);
+                atomicAdd(&g_wait_timeouts, 1ull);
                 break;
             }
             const uint32_t tile = blockIdx.x + k * gridDim.x;
@@ -336,7 +333,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
         }
         // the CTA's shared memory must outlive every copy issued into it
         for (uint32_t j = k > S ? k - S : 0; j < k; ++j)
-            if (!mbar_wait(&full[j % S], (j / S) & 1u)) atomicAdd(&g_bct_wait_timeouts, 1ull);
+            if (!mbar_wait(&full[j % S], (j / S) & 1u)) atomicAdd(&g_wait_timeouts, 1ull);
         return;
     }
 
@@ -347,7 +344,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
         const uint32_t s = k % S;
         if (live && !mbar_wait(&full[s], (k / S) & 1u)) {
             live = false;
-            atomicAdd(&g_bct_wait_timeouts, 1ull);
+            atomicAdd(&g_wait_timeouts, 1ull);
         }
         const uint8_t* stage = smem + s * L::kStage + rsub * (kTile * 2) + cc * 16;
         uint4 v[8];
@@ -467,9 +464,8 @@ extern "C" fp8_status_t fp8_quantize_block_cast_transpose(const void* x, fp8_dty
     return launch_bct<kE5M2>(xp, bf16, rows, cols, q_row, scale_inv_row, q_col, scale_inv_col, st);
 }
 
-extern "C" fp8_status_t fp8_wait_timeouts(unsigned long long* count) {
-    if (count == nullptr) return fail(FP8_ERR_INVALID_ARG, "fp8_wait_timeouts: count is NULL");
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(count, g_bct_wait_timeouts, sizeof *count);
-    return cuda_status(e, "fp8_wait_timeouts");
+namespace fp8q {
+fp8_status_t block_ct_wait_timeouts(unsigned long long* count) {
+    return cuda_status(cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof *count), "fp8_wait_timeouts");
 }
+}  // namespace fp8q

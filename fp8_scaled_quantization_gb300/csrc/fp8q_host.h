@@ -26,9 +26,14 @@ int sm_count();
 // Tensor map of a row-major [rows, cols] array of 16-bit elements at `base`
 // (16-byte aligned, cols * 2 a multiple of 16, rows and cols at most 2^32),
 // read in boxes of box_rows x box_cols elements into packed shared-memory rows
-// (no swizzle).  The encoder is the driver's, reached through the runtime.
+// (no swizzle).  Elements outside the array read as zero.  The encoder is the
+// driver's, reached through the runtime.
 fp8_status_t encode_tile_map_u16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
                                  int box_cols);
+
+// The wait-timeout counter of the pipelined kernels' translation unit on the
+// current device (no synchronisation: call after the device is idle).
+fp8_status_t block_ct_wait_timeouts(unsigned long long* count);
 
 // Workspace of (current device, stream) for per-CTA partials; nullptr on
 // failure (the error message is set).

@@ -9,6 +9,10 @@
 
 namespace fp8q {
 
+// Waits of this translation unit's pipelines that gave up (each unit that
+// includes this header has its own counter and a host reader for it).
+static __device__ unsigned long long g_wait_timeouts;
+
 // Tile pipelines: a producer warp copies input tiles into a ring of shared
 // memory stages with the bulk-copy (TMA) engine, each stage guarded by two
 // mbarriers -- `full` completes when the stage's bytes have landed, `empty`

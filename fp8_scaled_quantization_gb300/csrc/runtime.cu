@@ -129,6 +129,14 @@ int fp8_version(void) { return (FP8Q_VERSION_MAJOR << 16) | FP8Q_VERSION_MINOR; 
 
 unsigned long long fp8_launch_count(void) { return fp8q::g_launches.load(std::memory_order_relaxed); }
 
+fp8_status_t fp8_wait_timeouts(unsigned long long* count) {
+    using namespace fp8q;
+    if (count == nullptr) return fail(FP8_ERR_INVALID_ARG, "fp8_wait_timeouts: count is NULL");
+    fp8_status_t st = cuda_status(cudaDeviceSynchronize(), "fp8_wait_timeouts");
+    if (st == FP8_OK) st = block_ct_wait_timeouts(count);
+    return st;
+}
+
 fp8_status_t fp8_release_stream_workspace(void* stream) {
     using namespace fp8q;
     int dev = 0;
