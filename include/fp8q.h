@@ -330,8 +330,13 @@ fp8_status_t fp8_quantize_block(const void* x, fp8_dtype_t dtype, int64_t rows, 
  *       blockwise quantization of x^T, i.e. 128 x 1 blocks along the columns
  *       of x, written transposed.
  * Either direction may be NULL (codes and scales together).  BF16 inputs with
- * rows and cols multiples of 128 and 16-byte aligned x / codes use one kernel
- * over 128 x 128 tiles; other shapes use one guarded kernel per direction. */
+ * rows and cols multiples of 128 (each below 2^31) and 16-byte aligned x /
+ * codes use one persistent kernel over 128 x 128 tiles, which reads x through
+ * a tensor map (the driver's cuTensorMapEncodeTiled, reached through the
+ * runtime; FP8_ERR_CUDA if it is unavailable or refuses the shape) and holds
+ * 170 KB of shared memory per SM while it runs; its internal waits are
+ * bounded and counted by fp8_wait_timeouts.  Other shapes use one guarded
+ * kernel per direction. */
 fp8_status_t fp8_quantize_block_cast_transpose(const void* x, fp8_dtype_t dtype, int64_t rows, int64_t cols,
                                                fp8_format_t fmt, uint8_t* q_row, float* scale_inv_row,
                                                uint8_t* q_col, float* scale_inv_col, void* stream);
