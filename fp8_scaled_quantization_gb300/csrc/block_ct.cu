@@ -102,9 +102,10 @@ __device__ __forceinline__ uint2 row_codes(uint4 v, float scale, uint32_t rmax) 
 
 // Both directions of one 128 x 128 tile whose values are in v (thread tg of
 // the group: v[p] = row p * 16 + tg / 16, columns (tg % 16) * 8 .. + 7).  The
-// group's 256 threads synchronise on hardware barrier `bar`.  ROWS: q_row is
-// set (the columnwise-only form skips the rowwise products).
-template <int FMT, bool ROWS>
+// group's 256 threads synchronise on hardware barrier `bar`.  ROWS / COLS: the
+// rowwise / columnwise outputs are requested (a one-direction form skips the
+// other direction's reductions and products).
+template <int FMT, bool ROWS, bool COLS>
 __device__ __forceinline__ void bct_tile(const uint4 (&v)[8], const uint32_t* tab, TileSmem& ts, int bar, int tg,
                                          int64_t r0, int64_t c0, int64_t rows, int64_t cols, uint8_t* q_row,
                                          float* si_row, uint8_t* q_col, float* si_col) {
@@ -114,28 +115,30 @@ __device__ __forceinline__ void bct_tile(const uint4 (&v)[8], const uint32_t* ta
     // ---- rowwise 1 x 128 tiles: the half-warp of 16 lanes holds one row per p.
     // Rows p = 2j and 2j + 1 share a word (low / high 16 bits of their |x| bit
     // patterns), so one u16x2 shuffle-max reduction serves two rows.
-    uint32_t rm2[4];
+    uint32_t rm2[4] = {0u, 0u, 0u, 0u};
+    float rs = 1.0f, rsi = 1.0f;  // lane cc < 8: the scale of row p = cc
+    if (ROWS) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint4 a = v[2 * j], b = v[2 * j + 1];
-        const uint32_t ma = max_u16x2(max_u16x2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
-                                      max_u16x2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
-        const uint32_t mb = max_u16x2(max_u16x2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
-                                      max_u16x2(abs_bf16x2(b.z), abs_bf16x2(b.w)));
-        uint32_t w = max_u16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
+        for (int j = 0; j < 4; ++j) {
+            const uint4 a = v[2 * j], b = v[2 * j + 1];
+            const uint32_t ma = max_u16x2(max_u16x2(abs_bf16x2(a.x), abs_bf16x2(a.y)),
+                                          max_u16x2(abs_bf16x2(a.z), abs_bf16x2(a.w)));
+            const uint32_t mb = max_u16x2(max_u16x2(abs_bf16x2(b.x), abs_bf16x2(b.y)),
+                                          max_u16x2(abs_bf16x2(b.z), abs_bf16x2(b.w)));
+            uint32_t w = max_u16x2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-        rm2[j] = w;
+            for (int o = 8; o > 0; o >>= 1) w = max_u16x2(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+            rm2[j] = w;
+        }
+        // rm2[cc / 2] as a tree of selects: written as a loop of compares the
+        // compiler turns it into an indexed read of rm2 kept in local memory.
+        const uint32_t m01 = (cc & 2) ? rm2[1] : rm2[0], m23 = (cc & 2) ? rm2[3] : rm2[2];
+        const uint32_t mine2 = (cc & 4) ? m23 : m01;
+        block_scale_bf16<FMT>(tab, (cc & 1) ? (mine2 & 0xFFFF0000u) : (mine2 << 16), &rs, &rsi);
+        if (cc < 8) si_row[(r0 + cc * 16 + rsub) * nbr_row + (c0 >> 7)] = rsi;
     }
-    // rm2[cc / 2] as a tree of selects: written as a loop of compares the
-    // compiler turns it into an indexed read of rm2 kept in local memory.
-    const uint32_t m01 = (cc & 2) ? rm2[1] : rm2[0], m23 = (cc & 2) ? rm2[3] : rm2[2];
-    const uint32_t mine2 = (cc & 4) ? m23 : m01;
-    float rs, rsi;  // lane cc < 8: the scale of row p = cc
-    block_scale_bf16<FMT>(tab, (cc & 1) ? (mine2 & 0xFFFF0000u) : (mine2 << 16), &rs, &rsi);
-    if (ROWS && cc < 8) si_row[(r0 + cc * 16 + rsub) * nbr_row + (c0 >> 7)] = rsi;
 
-    if (q_col == nullptr) {  // rowwise codes only
+    if (!COLS) {  // rowwise codes only
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             const float scale = __shfl_sync(0xFFFFFFFFu, rs, (lane & 16) | p);
@@ -287,7 +290,7 @@ struct BctLayout {
 // a warp whose first lane timed out releases no more stages, so that no copy
 // is ever issued into a stage with one still in flight); every thread ends.
 // Registers: 17 warps per SM leave at most 96 per thread.
-template <int FMT, int NG, int S, bool ROWS>
+template <int FMT, int NG, int S, bool ROWS, bool COLS>
 __global__ void __maxnreg__(ROWS ? 88 : 96)
 block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int64_t cols, uint8_t* __restrict__ q_row,
                      float* __restrict__ si_row, uint8_t* __restrict__ q_col, float* __restrict__ si_col) {
@@ -353,7 +356,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
         __syncwarp();
         if (lane == 0 && live) mbar_arrive(&empty[s]);  // never release a stage whose copy may be in flight
         const uint32_t tile = blockIdx.x + k * gridDim.x;
-        bct_tile<FMT, ROWS>(v, tab, ts, 1 + g, tg, (int64_t)(tile / nbr_row) * kTile, (int64_t)(tile % nbr_row) * kTile, rows,
+        bct_tile<FMT, ROWS, COLS>(v, tab, ts, 1 + g, tg, (int64_t)(tile / nbr_row) * kTile, (int64_t)(tile % nbr_row) * kTile, rows,
                       cols, q_row, si_row, q_col, si_col);
     }
 }
@@ -409,7 +412,9 @@ fp8_status_t launch_bct(const uint8_t* x, bool bf16, int64_t rows, int64_t cols,
         if (es != FP8_OK) return es;
         const int64_t ntiles = (rows / kTile) * (cols / kTile);
         const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
-        auto kernel = q_row != nullptr ? block_ct_pipe_kernel<FMT, NG, S, true> : block_ct_pipe_kernel<FMT, NG, S, false>;
+        auto kernel = q_row == nullptr   ? block_ct_pipe_kernel<FMT, NG, S, false, true>
+                      : q_col == nullptr ? block_ct_pipe_kernel<FMT, NG, S, true, false>
+                                         : block_ct_pipe_kernel<FMT, NG, S, true, true>;
         return launch_smem(w, kernel, dim3((unsigned)grid), dim3(NG * 256 + 32), (size_t)BctLayout<NG, S>::kBytes, st,
                            xmap, rows, cols, q_row, si_row, q_col, si_col);
     }
