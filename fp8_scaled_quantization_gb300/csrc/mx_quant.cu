@@ -109,6 +109,17 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
     // their |x| bit patterns), so one u16x2 shuffle-max over the 4 lanes of a
     // 32-element block serves both rows.  vrows is a multiple of 32, so the
     // rows of a pair are both inside the tensor or both outside.
+    // Stage the tile for the column pass first, so that the barrier does not
+    // wait for the other warps' row passes.
+    if (q_col) {
+#pragma unroll
+        for (int p = 0; p < kLoads; ++p) {
+            if (p * 16 >= vrows) break;  // uniform over the CTA
+            const int r = p * 16 + rsub;
+            tile[r * 16 + mx_chunk(r, cc)] = v[p];
+        }
+        __syncthreads();
+    }
     uint32_t rb2[kLoads / 2] = {};
     if (q_row) {
 #pragma unroll
@@ -143,10 +154,8 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
             stg_stream(qr + ((Off)r * ocols + (Off)(cc * 8)), codes);
             if ((lane & 3) == 0) sr[(Off)r * nbr + (Off)(cc >> 2)] = (uint8_t)code;
         }
-        if (q_col) tile[r * 16 + mx_chunk(r, cc)] = v[p];
     }
     if (!q_col) return;
-    __syncthreads();
     const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
     const int g = t & 7;  // rows 16 g .. 16 g + 15
     const bool live = g * 16 < vrows;  // lanes g and g ^ 1 agree (vrows % 32 == 0)
