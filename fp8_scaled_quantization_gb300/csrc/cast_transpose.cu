@@ -57,8 +57,10 @@ __device__ __forceinline__ uint4 dequant8_bf16(uint32_t lo, uint32_t hi, float s
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const uint32_t h01 = fp8x2_to_f16x2<FMT>(w[i] & 0xFFFFu), h23 = fp8x2_to_f16x2<FMT>(w[i] >> 16);
-        out[2 * i] = f32x2_to_bf16x2(__fmul_rn(f16_lo_to_f32(h01), si), __fmul_rn(f16_hi_to_f32(h01), si));
-        out[2 * i + 1] = f32x2_to_bf16x2(__fmul_rn(f16_lo_to_f32(h23), si), __fmul_rn(f16_hi_to_f32(h23), si));
+        const float2 p01 = fmul2_rn(f16_lo_to_f32(h01), f16_hi_to_f32(h01), si);
+        const float2 p23 = fmul2_rn(f16_lo_to_f32(h23), f16_hi_to_f32(h23), si);
+        out[2 * i] = f32x2_to_bf16x2(p01.x, p01.y);
+        out[2 * i + 1] = f32x2_to_bf16x2(p23.x, p23.y);
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
