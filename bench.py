@@ -574,7 +574,7 @@ def flush_buffers(dev):
 
 def time_flushed(fn, dev, reps=20, bufs=None):
     """One call at a time between two events, the L2 flushed before every rep
-    (EXTRAS_TIMING); returns (median, min, max) in us over `reps` reps."""
+    (EXTRAS_TIMING); returns (median, min, max, mean) in us over `reps` reps."""
     import torch
     flush, clean = bufs or flush_buffers(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -588,7 +588,7 @@ def time_flushed(fn, dev, reps=20, bufs=None):
         torch.cuda.synchronize()
         if r >= 2:
             ts.append(e0.elapsed_time(e1) * 1e3)
-    return statistics.median(ts), min(ts), max(ts)
+    return statistics.median(ts), min(ts), max(ts), statistics.mean(ts)
 
 
 def time_cold(fn, dev):
@@ -656,12 +656,14 @@ def compare_parity(snap, ref):
 
 EXTRAS_TIMING = ("CUDA events around each call on the launching stream; before every rep (outside the "
                  "events) a 256 MB buffer is rewritten and then a second 256 MB buffer is read, so the inputs "
-                 "are out of L2 and the flush's dirty lines are written back before the timed call")
+                 "are out of L2 and the flush's dirty lines are written back before the timed call; one "
+                 "launch between two events reads in steps of about 2.05 us on these GPUs, so the median "
+                 "moves by whole steps and the mean resolves below one")
 
 
 def run_extras(inp, peak, reps=20):
     """Kernels beyond the five workloads, each timed on its own (EXTRAS_TIMING),
-    median of `reps` reps with min and max.  The read after the rewrite
+    median of `reps` reps with min, max and mean.  The read after the rewrite
     matters: a rewrite alone leaves the L2 full of dirty lines, and the timed
     kernel would pay for writing them back."""
     import torch
@@ -673,12 +675,14 @@ def run_extras(inp, peak, reps=20):
         return time_flushed(fn, dev, reps, bufs)
 
     def row(t, nbytes, what):
-        us, lo, hi = t if isinstance(t, tuple) else (t, None, None)
+        us, lo, hi, mean = t if isinstance(t, tuple) else (t, None, None, None)
         gbs = nbytes / (us * 1e-6) / 1e9
         r = {"what": what, "us": round(us, 2), "bytes": int(nbytes), "gbs": round(gbs, 1),
              "frac": round(gbs / peak, 4)}
         if lo is not None:
-            r.update({"median_us": round(us, 2), "min_us": round(lo, 2), "max_us": round(hi, 2), "reps": reps})
+            r.update({"median_us": round(us, 2), "min_us": round(lo, 2), "max_us": round(hi, 2),
+                      "mean_us": round(mean, 2), "mean_frac": round(nbytes / (mean * 1e-6) / 1e9 / peak, 4),
+                      "reps": reps})
         return r
 
     out = {}
