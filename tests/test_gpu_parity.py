@@ -546,6 +546,29 @@ def test_cuda_graph_capture_and_replay(cuda, oracle):
         assert np.array_equal(q_row.cpu().numpy(), wr) and np.array_equal(q_col.cpu().numpy(), wc)
 
 
+def test_block_cast_transpose_in_a_captured_graph(cuda, oracle):
+    """The tensor-map kernel captured once (its map, built on the host from
+    x's address, is a kernel argument of the graph node) and replayed while x
+    changes in place."""
+    x = random_input((512, 768), torch.bfloat16, 23, cuda)
+    q_row = torch.empty((512, 768), dtype=torch.uint8, device=cuda)
+    s_row = torch.empty((512, 6), dtype=torch.float32, device=cuda)
+    q_col = torch.empty((768, 512), dtype=torch.uint8, device=cuda)
+    s_col = torch.empty((768, 4), dtype=torch.float32, device=cuda)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fq.fp8_quantize_block_cast_transpose(x, E4M3, q_row, s_row, q_col, s_col)
+    for _ in range(3):
+        x.mul_(1.5)
+        graph.replay()
+        torch.cuda.synchronize()
+        xb = host_bits(x)
+        wq, ws = oracle.quantize_block(xb, 1, 128, E4M3)
+        assert np.array_equal(q_row.cpu().numpy(), wq) and np.array_equal(s_row.cpu().numpy(), ws)
+        wqt, wst = oracle.quantize_block(np.ascontiguousarray(xb.T), 1, 128, E4M3)
+        assert np.array_equal(q_col.cpu().numpy(), wqt) and np.array_equal(s_col.cpu().numpy(), wst)
+
+
 def test_reducing_casts_in_a_captured_graph(cuda, oracle):
     """The reducing casts and their finalize replayed from a graph, with the
     stream workspace created inside the capture."""
