@@ -25,6 +25,7 @@ SIGNATURES = {
     "fp8_version": (c_i32, []),
     "fp8_launch_count": (c_u64, []),
     "fp8_wait_timeouts": (c_i32, [c_vp]),
+    "fp8_test_drop_tile_copy": (c_i32, [c_i32]),
     "fp8_release_stream_workspace": (c_i32, [c_vp]),
     "fp8_amax": (c_i32, [c_vp, c_i32, c_i64, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "fp8_update_scale_delayed": (c_i32, [c_vp, c_i32, c_i64, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),

@@ -270,6 +270,11 @@ transpose:
     }
 }
 
+// Test hook (fp8_test_drop_tile_copy): the copying thread of every CTA skips
+// the copy of its tile number g_drop_tile, so that the waits on that stage
+// expire; -1 (the default) skips none.
+__device__ int g_drop_tile = -1;
+
 // Shared memory of the pipelined kernel: S stages of one 128 x 128 BF16 tile
 // (32 KB, rows of 256 bytes), NG group areas, the scale tables, the barriers.
 template <int NG, int S>
@@ -322,6 +327,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
 
     if (warp == NG * 8) {  // producer: one thread issues the tile copies
         if (lane != 0) return;
+        const int drop = g_drop_tile;
         uint32_t k = 0;
         for (; k < n_my; ++k) {
             const uint32_t s = k % S;
@@ -329,6 +335,7 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
                 atomicAdd(&g_wait_timeouts, 1ull);
                 break;
             }
+            if ((int)k == drop) continue;
             const uint32_t tile = blockIdx.x + k * gridDim.x;
             mbar_arrive_expect_tx(&full[s], L::kStage);
             tma_load_2d(smem + s * L::kStage, &xmap, (int)(tile % nbr_row) * kTile, (int)(tile / nbr_row) * kTile,
@@ -474,3 +481,7 @@ fp8_status_t block_ct_wait_timeouts(unsigned long long* count) {
     return cuda_status(cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof *count), "fp8_wait_timeouts");
 }
 }  // namespace fp8q
+
+extern "C" fp8_status_t fp8_test_drop_tile_copy(int tile) {
+    return cuda_status(cudaMemcpyToSymbol(g_drop_tile, &tile, sizeof tile), "fp8_test_drop_tile_copy");
+}

@@ -59,14 +59,19 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity to complete; gives up
-// after about two seconds (a copy that never lands) and returns false.
+// after about two seconds of %globaltimer (a copy that never lands) and
+// returns false.  A cap on the number of polls bounds the wait even if the
+// timer did not advance.
 constexpr uint64_t kMbarWaitLimitNs = 2000000000ull;
+constexpr uint32_t kMbarWaitMaxPolls = 1u << 24;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
+    for (uint32_t i = 0; i < kMbarWaitMaxPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > kMbarWaitLimitNs) return false;
-    return true;
+    }
+    return false;
 }
 
 // The box of tensor map `map` at element coordinates (x, y) -- x innermost,

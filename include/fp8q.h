@@ -122,6 +122,15 @@ unsigned long long fp8_launch_count(void);
  * launch.  FP8_ERR_INVALID_ARG if count is NULL. */
 fp8_status_t fp8_wait_timeouts(unsigned long long* count);
 
+/* Test hook for the bounded waits above: from the next launch on, the thread
+ * that copies tiles in each CTA of the blockwise cast-transpose's tiled path
+ * skips the copy of its tile number `tile` (counted from 0 per CTA; -1, the
+ * default, skips none), so that every wait on that stage expires after its
+ * limit: the kernel still ends, fp8_wait_timeouts grows, and the outputs of
+ * those launches are garbage.  For tests of the error path only; it
+ * synchronises with the device. */
+fp8_status_t fp8_test_drop_tile_copy(int tile);
+
 /* Frees the reduction workspace (96 KB) that the calls made on `stream` on the
  * current device, after waiting for the work queued on that stream.  A later
  * reducing call on the stream allocates a new one.  Returns FP8_OK when there

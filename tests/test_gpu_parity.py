@@ -680,6 +680,36 @@ def test_block_cast_transpose_tile_ring(cuda, oracle, shape, direction):
         assert np.array_equal(q_col.cpu().numpy(), wqt)
 
 
+@pytest.mark.parametrize("shape", [(256, 256), (1024, 12160)])
+def test_block_cast_transpose_expired_waits_end_and_are_counted(cuda, oracle, native_lib, shape):
+    """The bounded waits of the tiled path, made to expire: with the copy of
+    each CTA's first tile skipped (test hook), the launch still ends (its
+    consumers give up after their limit; with 760 tiles the copying thread
+    also gives up on a stage that is never released), the expired waits are
+    counted, and the next launch on the same context is exact again."""
+    rows, cols = shape
+    x = random_input(shape, torch.bfloat16, 31, cuda)
+    q_row = torch.empty((rows, cols), dtype=torch.uint8, device=cuda)
+    s_row = torch.empty((rows, cols // 128), dtype=torch.float32, device=cuda)
+    q_col = torch.empty((cols, rows), dtype=torch.uint8, device=cuda)
+    s_col = torch.empty((cols, rows // 128), dtype=torch.float32, device=cuda)
+    before = fq.wait_timeouts()
+    assert native_lib.fp8_test_drop_tile_copy(0) == 0
+    try:
+        fq.fp8_quantize_block_cast_transpose(x, E4M3, q_row, s_row, q_col, s_col)
+        expired = fq.wait_timeouts()
+    finally:
+        assert native_lib.fp8_test_drop_tile_copy(-1) == 0
+    assert expired > before
+    fq.fp8_quantize_block_cast_transpose(x, E4M3, q_row, s_row, q_col, s_col)
+    assert fq.wait_timeouts() == expired
+    xb = host_bits(x)
+    wq, ws = oracle.quantize_block(xb, 1, 128, E4M3)
+    assert np.array_equal(q_row.cpu().numpy(), wq) and np.array_equal(s_row.cpu().numpy(), ws)
+    wqt, wst = oracle.quantize_block(np.ascontiguousarray(xb.T), 1, 128, E4M3)
+    assert np.array_equal(q_col.cpu().numpy(), wqt) and np.array_equal(s_col.cpu().numpy(), wst)
+
+
 def test_block_cast_transpose_tile_without_specials(cuda, oracle):
     """A 512 x 512 BF16 tensor with no Inf / NaN: every tile takes the paired
     two-value conversion of the columnwise codes."""
