@@ -47,6 +47,26 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
     return r;
 }
 
+// Four fp32 -> four FP8 codes in one word (a in bits 0-7, b 8-15, c 16-23,
+// d 24-31): two two-value converts written into the halves of one register.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
+    uint32_t r;
+    if constexpr (FMT == kE4M3)
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
 // Two FP8 codes (low 16 bits of `c2`) -> two exact f16 values (f16x2).
 template <int FMT>
 __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t c2) {
@@ -246,12 +266,8 @@ __device__ __forceinline__ Codes8 cvt_bf16x8(uint4 v, float scale, uint32_t* abs
     const float2 p1 = fmul2_rn(bf16lo(v.y), bf16hi(v.y), scale);
     const float2 p2 = fmul2_rn(bf16lo(v.z), bf16hi(v.z), scale);
     const float2 p3 = fmul2_rn(bf16lo(v.w), bf16hi(v.w), scale);
-    uint32_t c0 = cvt2<FMT>(p0.x, p0.y);
-    uint32_t c1 = cvt2<FMT>(p1.x, p1.y);
-    uint32_t c2 = cvt2<FMT>(p2.x, p2.y);
-    uint32_t c3 = cvt2<FMT>(p3.x, p3.y);
-    c.lo = c0 | (c1 << 16);
-    c.hi = c2 | (c3 << 16);
+    c.lo = cvt4<FMT>(p0.x, p0.y, p1.x, p1.y);
+    c.hi = cvt4<FMT>(p2.x, p2.y, p3.x, p3.y);
     *absmax = max_u16x2(max_u16x2(abs_bf16x2(v.x), abs_bf16x2(v.y)),
                         max_u16x2(abs_bf16x2(v.z), abs_bf16x2(v.w)));
     return c;
@@ -266,8 +282,8 @@ __device__ __forceinline__ Codes8 cvt_bf16x8_nomax(uint4 v, float scale) {
     const float2 p1 = fmul2_rn(bf16lo(v.y), bf16hi(v.y), scale);
     const float2 p2 = fmul2_rn(bf16lo(v.z), bf16hi(v.z), scale);
     const float2 p3 = fmul2_rn(bf16lo(v.w), bf16hi(v.w), scale);
-    c.lo = cvt2<FMT>(p0.x, p0.y) | (cvt2<FMT>(p1.x, p1.y) << 16);
-    c.hi = cvt2<FMT>(p2.x, p2.y) | (cvt2<FMT>(p3.x, p3.y) << 16);
+    c.lo = cvt4<FMT>(p0.x, p0.y, p1.x, p1.y);
+    c.hi = cvt4<FMT>(p2.x, p2.y, p3.x, p3.y);
     return c;
 }
 
@@ -323,12 +339,10 @@ template <int FMT>
 __device__ __forceinline__ uint32_t cvt_f32x4(float4 v, float scale, uint32_t* absmax) {
     const float2 p0 = fmul2_rn(v.x, v.y, scale);
     const float2 p1 = fmul2_rn(v.z, v.w, scale);
-    uint32_t c0 = cvt2<FMT>(p0.x, p0.y);
-    uint32_t c1 = cvt2<FMT>(p1.x, p1.y);
     uint32_t a = __float_as_uint(v.x) & 0x7FFFFFFFu, b = __float_as_uint(v.y) & 0x7FFFFFFFu;
     uint32_t c = __float_as_uint(v.z) & 0x7FFFFFFFu, d = __float_as_uint(v.w) & 0x7FFFFFFFu;
     *absmax = umax(umax(a, b), umax(c, d));
-    return c0 | (c1 << 16);
+    return cvt4<FMT>(p0.x, p0.y, p1.x, p1.y);
 }
 
 // Redo 4 fp32 elements exactly (by value, as fixup_bf16x8_exact).

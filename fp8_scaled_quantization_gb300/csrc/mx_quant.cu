@@ -184,15 +184,16 @@ mx_tile_kernel(const uint8_t* __restrict__ x, int64_t rows, int64_t cols, uint8_
             } else {
                 code = mx_scale_code<FMT>(bits);
                 const float mul = mx_multiplier(code);
-                uint32_t c2[8];  // codes of rows 2 i, 2 i + 1
+                uint32_t c4[4];  // codes of rows 4 i .. 4 i + 3
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float2 f = j ? fmul2_rn(bf16hi(w[2 * i]), bf16hi(w[2 * i + 1]), mul)
-                                       : fmul2_rn(bf16lo(w[2 * i]), bf16lo(w[2 * i + 1]), mul);
-                    c2[i] = cvt2<FMT>(f.x, f.y);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = j ? fmul2_rn(bf16hi(w[4 * i]), bf16hi(w[4 * i + 1]), mul)
+                                       : fmul2_rn(bf16lo(w[4 * i]), bf16lo(w[4 * i + 1]), mul);
+                    const float2 g = j ? fmul2_rn(bf16hi(w[4 * i + 2]), bf16hi(w[4 * i + 3]), mul)
+                                       : fmul2_rn(bf16lo(w[4 * i + 2]), bf16lo(w[4 * i + 3]), mul);
+                    c4[i] = cvt4<FMT>(f.x, f.y, g.x, g.y);
                 }
-                codes = make_uint4(__byte_perm(c2[0], c2[1], 0x5410), __byte_perm(c2[2], c2[3], 0x5410),
-                                   __byte_perm(c2[4], c2[5], 0x5410), __byte_perm(c2[6], c2[7], 0x5410));
+                codes = make_uint4(c4[0], c4[1], c4[2], c4[3]);
             }
             const Off c = (Off)(2 * cp + j);  // column inside the tile
             if (live) {
