@@ -363,8 +363,8 @@ block_ct_pipe_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int
         __syncwarp();
         if (lane == 0 && live) mbar_arrive(&empty[s]);  // never release a stage whose copy may be in flight
         const uint32_t tile = blockIdx.x + k * gridDim.x;
-        bct_tile<FMT, ROWS, COLS>(v, tab, ts, 1 + g, tg, (int64_t)(tile / nbr_row) * kTile, (int64_t)(tile % nbr_row) * kTile, rows,
-                      cols, q_row, si_row, q_col, si_col);
+        const int64_t r0 = (int64_t)(tile / nbr_row) * kTile, c0 = (int64_t)(tile % nbr_row) * kTile;
+        bct_tile<FMT, ROWS, COLS>(v, tab, ts, 1 + g, tg, r0, c0, rows, cols, q_row, si_row, q_col, si_col);
     }
 }
 
@@ -411,7 +411,8 @@ fp8_status_t launch_bct(const uint8_t* x, bool bf16, int64_t rows, int64_t cols,
                         uint8_t* q_col, float* si_col, cudaStream_t st) {
     const char* w = "fp8_quantize_block_cast_transpose";
     const bool fast = bf16 && rows % kTile == 0 && cols % kTile == 0 && aligned16(x) && (!q_row || aligned16(q_row)) &&
-                      (!q_col || aligned16(q_col)) && (rows / kTile) * (cols / kTile) <= 0x7FFFFFFF && rows <= 0x7FFFFFFF && cols <= 0x7FFFFFFF;
+                      (!q_col || aligned16(q_col)) && (rows / kTile) * (cols / kTile) <= 0x7FFFFFFF &&
+                      rows <= 0x7FFFFFFF && cols <= 0x7FFFFFFF;
     if (fast) {
         constexpr int NG = kGroups, S = kStages;
         CUtensorMap xmap;
@@ -465,7 +466,8 @@ extern "C" fp8_status_t fp8_quantize_block_cast_transpose(const void* x, fp8_dty
     if (rows == 0 || cols == 0) return FP8_OK;
     if (x == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: x is NULL", fn);
     if (q_row == nullptr && q_col == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output requested", fn);
-    if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype)) return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
+    if (reinterpret_cast<uintptr_t>(x) % dtype_size(dtype))
+        return fail(FP8_ERR_INVALID_ARG, "%s: x not element-aligned", fn);
     if ((scale_inv_row && reinterpret_cast<uintptr_t>(scale_inv_row) % 4) ||
         (scale_inv_col && reinterpret_cast<uintptr_t>(scale_inv_col) % 4))
         return fail(FP8_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", fn);
