@@ -13,8 +13,8 @@ namespace fp8q {
 // includes this header has its own counter and a host reader for it).
 static __device__ unsigned long long g_wait_timeouts;
 
-// Tile pipelines: a producer warp copies input tiles into a ring of shared
-// memory stages with the bulk-copy (TMA) engine, each stage guarded by two
+// Tile pipelines: one producer thread copies input tiles into a ring of
+// shared memory stages with the bulk-copy (TMA) engine, each stage guarded by two
 // mbarriers -- `full` completes when the stage's bytes have landed, `empty`
 // when its consumers have read it -- so that reads of the next tiles stay in
 // flight while consumer warps work on the current one.
