@@ -755,26 +755,30 @@ def run_extras(inp, peak, reps=20):
                                   "CUDA graph, warm L2; compulsory 3 B/element")
     # W1 as it runs in the step: issued right behind a large kernel, so its
     # launch overlaps that kernel's tail and its input is out of L2; the time
-    # of (large kernel + W1) minus that of the large kernel alone, medians of 20
+    # of (large kernel + W1) minus that of the large kernel alone, means of 60
+    # (the event clock reads in steps of about 2.05 us, which a median keeps
+    # and a mean resolves), the two kinds of rep interleaved
     big = torch.empty(64 << 20, dtype=torch.float32, device=dev)
 
-    def pair_us(with_w1):
-        ts = []
-        for r in range(22):
+    def pair_times():
+        ts = {True: [], False: []}
+        for r in range(124):
+            with_w1 = bool(r & 1)
             e0.record()
             big.mul_(1.0)
             if with_w1:
                 fq.fp8_quantize_current(x1, fq.E4M3, q1, 0, a1, s1, si1)
             e1.record()
             torch.cuda.synchronize()
-            if r >= 2:
-                ts.append(e0.elapsed_time(e1) * 1e3)
-        return statistics.median(ts)
+            if r >= 4:
+                ts[with_w1].append(e0.elapsed_time(e1) * 1e3)
+        return statistics.mean(ts[True]), statistics.mean(ts[False])
 
-    us = pair_us(True) - pair_us(False)
+    with_w1_us, without_us = pair_times()
+    us = with_w1_us - without_us
     out["w1_behind_large_kernel"] = row(us, x1.numel() * 3, "W1 current scaling issued right behind a 256 MB "
                                         "kernel (launch overlapped, input out of L2): (kernel + W1) - kernel, "
-                                        "medians of 20; compulsory 3 B/element")
+                                        "means of 60, interleaved; compulsory 3 B/element")
     del big
     del q1
     # 64 expert-sized tensors: grouped current scaling vs per-tensor calls
